@@ -1,0 +1,496 @@
+// gdr_chunked.cu -- the chunked (three-kernel) form of the gated delta rule
+// forward on CUDA cores, fp32 arithmetic throughout.
+//
+// Kernel order follows the pages' forward chain (KCP handbook, section on the
+// debug-script layout: fwd_intra -> wy -> fwd_h -> o):
+//   chunk_index_kernel  cu_seqlens -> (sequence, chunk) map, int64
+//   prepare_kernel      per (chunk, value head): L2 norm of k, gate cumsum,
+//                       A = tril(beta K K^T * decay, -1), (I + A)^-1 applied by
+//                       forward substitution to give w and u
+//   fwd_h_kernel        per (sequence, value head, V-tile), sequential over
+//                       chunks: h (state entering the chunk), v_new = u - w h,
+//                       h <- exp(G_C) h + (K * exp(G_C - G))^T v_new
+//   fwd_o_kernel        per (chunk, value head): o = (q * exp G) h + P v_new
+//                       with P = tril(q k^T * decay) (diagonal included)
+//
+// Decay factors are always formed as exp(G_i - G_j) with i >= j, so every
+// exponent is <= 0 and nothing overflows, whatever the gate values.
+// All address arithmetic is int64 (coverage guide, section 四).
+#include <algorithm>
+
+#include "gdr_device.cuh"
+#include "gdr_internal.h"
+
+namespace gdr {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kBVh = 32;  // V-tile of the state scan
+
+// --------------------------------------------------------------------------
+// chunk index: one block.  Validates cu_seqlens (non-decreasing, cu[0] = 0,
+// cu[N] = T); on a violation every offset is -1, every index row is -1 and the
+// status word records GDR_ERR_SEQLENS, so the later kernels touch nothing.
+// --------------------------------------------------------------------------
+__global__ void chunk_index_kernel(const int64_t *__restrict__ cu, int64_t N, int64_t T, int C,
+                                   int64_t nt_max, int64_t *__restrict__ chunk_indices,
+                                   int64_t *__restrict__ chunk_offsets, int *status) {
+  __shared__ long long warp_tot[kThreads / 32];
+  __shared__ long long carry_s;
+  __shared__ int bad_s;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    carry_s = 0;
+    bad_s = 0;
+  }
+  __syncthreads();
+  if (cu) {
+    for (int64_t n = tid; n < N; n += blockDim.x)
+      if (cu[n + 1] < cu[n]) bad_s = 1;
+    if (tid == 0 && (cu[0] != 0 || cu[N] != T)) bad_s = 1;
+  }
+  __syncthreads();
+  if (bad_s) {
+    for (int64_t n = tid; n <= N; n += blockDim.x) chunk_offsets[n] = -1;
+    if (chunk_indices)
+      for (int64_t i = tid; i < 2 * nt_max; i += blockDim.x) chunk_indices[i] = -1;
+    if (tid == 0) raise_status(status, GDR_ERR_SEQLENS);
+    return;
+  }
+  for (int64_t base = 0; base < N; base += blockDim.x) {
+    const int64_t n = base + tid;
+    long long nc = 0;
+    if (n < N) {
+      const int64_t len = cu ? cu[n + 1] - cu[n] : T;
+      nc = (len + C - 1) / C;
+    }
+    long long x = nc;  // inclusive warp scan
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      long long y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    long long before = 0, total = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      if (w < warp) before += warp_tot[w];
+      total += warp_tot[w];
+    }
+    const long long excl = carry_s + before + x - nc;
+    if (n < N) {
+      chunk_offsets[n] = excl;
+      if (chunk_indices)
+        for (long long j = 0; j < nc; ++j) {
+          chunk_indices[2 * (excl + j)] = n;
+          chunk_indices[2 * (excl + j) + 1] = j;
+        }
+    }
+    __syncthreads();
+    if (tid == 0) carry_s += total;
+    __syncthreads();
+  }
+  const long long nt = carry_s;
+  if (tid == 0) chunk_offsets[N] = nt;
+  if (chunk_indices)
+    for (int64_t i = nt + tid; i < nt_max; i += blockDim.x) {
+      chunk_indices[2 * i] = -1;
+      chunk_indices[2 * i + 1] = -1;
+    }
+}
+
+// Maps a chunk row to (sequence, chunk-in-sequence); false if the row is unused.
+__device__ __forceinline__ bool chunk_coords(const int64_t *chunk_indices, int64_t chunk, int64_t T, int C,
+                                             int64_t *n, int64_t *j) {
+  if (chunk_indices) {
+    *n = chunk_indices[2 * chunk];
+    *j = chunk_indices[2 * chunk + 1];
+    return *n >= 0;
+  }
+  const int64_t ncs = (T + C - 1) / C;
+  *n = chunk / ncs;
+  *j = chunk % ncs;
+  return true;
+}
+
+// Loads one token row of q or k (head hq) into smem, L2-normalized if asked.
+// Called by a whole warp; rows past the chunk's end are zero.
+template <typename Tin>
+__device__ __forceinline__ void load_row_normed(const Tin *__restrict__ x, int64_t tok, int64_t H, int64_t hq,
+                                                int64_t K, bool valid, bool l2, float *dst, int lane) {
+  float r[8];
+  float ss = 0.f;
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const int64_t d = lane + 32 * m;
+    r[m] = (valid && d < K) ? to_f32(x[(tok * H + hq) * K + d]) : 0.f;
+    ss += r[m] * r[m];
+  }
+  float scale = 1.f;
+  if (l2) scale = rsqrtf(warp_sum(ss) + kL2Eps);
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const int64_t d = lane + 32 * m;
+    if (d < K) dst[d] = r[m] * scale;
+  }
+}
+
+// --------------------------------------------------------------------------
+// prepare: grid (nt_max, HV)
+// smem: ks[C*K] | gam[C*K or C] | bet[C] | A[C*C]
+// --------------------------------------------------------------------------
+template <typename Tin, int C, bool PER_K>
+__global__ void __launch_bounds__(kThreads) prepare_kernel(
+    const Tin *__restrict__ k, const Tin *__restrict__ v, const float *__restrict__ g,
+    const Tin *__restrict__ beta, const int64_t *__restrict__ cu, const int64_t *__restrict__ chunk_indices,
+    int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V, int l2, float *__restrict__ gcum,
+    float *__restrict__ w, float *__restrict__ u) {
+  extern __shared__ float smem[];
+  float *ks = smem;
+  float *gam = ks + C * K;
+  float *bet = gam + (PER_K ? C * K : C);
+  float *A = bet + C;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t chunk = blockIdx.x, hv = blockIdx.y;
+  int64_t n, j;
+  if (!chunk_coords(chunk_indices, chunk, T, C, &n, &j)) return;
+  const SeqRange sr = seq_range(cu, n, T);
+  const int64_t t0 = sr.bos + j * C;
+  const int Lc = (int)(sr.eos - t0 < (int64_t)C ? sr.eos - t0 : (int64_t)C);
+  const int64_t hq = hv / (HV / H);
+
+  for (int i = warp; i < C; i += kWarps) load_row_normed(k, t0 + i, H, hq, K, i < Lc, l2, ks + i * K, lane);
+  // gate cumsum within the chunk: load every g in parallel, then scan in smem
+  const int64_t gw = PER_K ? K : 1;
+  for (int64_t e = tid; e < C * gw; e += kThreads) {
+    const int64_t i = e / gw, d = e % gw;
+    gam[e] = i < Lc ? g[((t0 + i) * HV + hv) * gw + d] : 0.f;
+  }
+  for (int i = tid; i < C; i += kThreads) bet[i] = i < Lc ? to_f32(beta[(t0 + i) * HV + hv]) : 0.f;
+  __syncthreads();
+  for (int64_t d = tid; d < gw; d += kThreads) {
+    float s = 0.f;
+    for (int i = 0; i < C; ++i) {
+      s += gam[i * gw + d];
+      gam[i * gw + d] = s;
+    }
+  }
+  __syncthreads();
+  for (int64_t e = tid; e < Lc * gw; e += kThreads) {
+    const int64_t i = e / gw, d = e % gw;
+    gcum[((t0 + i) * HV + hv) * gw + d] = gam[e];
+  }
+
+  // A_ij = beta_i sum_d k_id k_jd exp(G_id - G_jd), i > j
+  for (int p = warp; p < C * C; p += kWarps) {
+    const int i = p / C, jj = p % C;
+    if (jj >= i || i >= Lc) {
+      if (lane == 0) A[p] = 0.f;
+      continue;
+    }
+    float s = 0.f;
+    for (int64_t d = lane; d < K; d += 32) {
+      float t = ks[i * K + d] * ks[jj * K + d];
+      if (PER_K) t *= expf(gam[i * K + d] - gam[jj * K + d]);
+      s += t;
+    }
+    s = warp_sum(s);
+    if (lane == 0) A[p] = bet[i] * s * (PER_K ? 1.f : expf(gam[i] - gam[jj]));
+  }
+  __syncthreads();
+
+  // (I + A) x = rhs by forward substitution, one column per thread:
+  // columns [0, K) give w (rhs beta_i exp(G_i) k_i), columns [K, K+V) give u (rhs beta_i v_i)
+  for (int64_t col = tid; col < K + V; col += kThreads) {
+    float x[C];
+    const bool is_w = col < K;
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+      float rhs;
+      if (is_w) {
+        rhs = bet[i] * ks[i * K + col] * expf(PER_K ? gam[i * K + col] : gam[i]);
+      } else {
+        rhs = i < Lc ? bet[i] * to_f32(v[((t0 + i) * HV + hv) * V + (col - K)]) : 0.f;
+      }
+      float acc = rhs;
+#pragma unroll
+      for (int jj = 0; jj < i; ++jj) acc = fmaf(-A[i * C + jj], x[jj], acc);
+      x[i] = acc;
+    }
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+      if (i < Lc) {
+        if (is_w) w[((t0 + i) * HV + hv) * K + col] = x[i];
+        else u[((t0 + i) * HV + hv) * V + (col - K)] = x[i];
+      }
+    }
+  }
+}
+
+// --------------------------------------------------------------------------
+// fwd_h: grid (N, HV, ceil(V / 32)), sequential over the sequence's chunks.
+// smem: hs[K*32] | ws[C*K] | kt[C*K] | vn[C*32] | gl[K]
+// --------------------------------------------------------------------------
+template <typename Tin, int C, bool PER_K>
+__global__ void __launch_bounds__(kThreads) fwd_h_kernel(
+    const Tin *__restrict__ k, const float *__restrict__ w, const float *__restrict__ u,
+    const float *__restrict__ gcum, const float *__restrict__ h0, const int64_t *__restrict__ cu,
+    const int64_t *__restrict__ chunk_offsets, int64_t N, int64_t T, int64_t H, int64_t HV, int64_t K,
+    int64_t V, int l2, float *__restrict__ h, float *__restrict__ v_new, float *__restrict__ ht) {
+  extern __shared__ float smem[];
+  float *hs = smem;
+  float *ws = hs + K * kBVh;
+  float *kt = ws + C * K;
+  float *vn = kt + C * K;
+  float *gl = vn + C * kBVh;
+  if (chunk_offsets && chunk_offsets[N] < 0) return;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t n = blockIdx.x, hv = blockIdx.y, v0 = (int64_t)blockIdx.z * kBVh;
+  const int64_t hq = hv / (HV / H);
+  const SeqRange sr = seq_range(cu, n, T);
+  const int64_t nch = (sr.eos - sr.bos + C - 1) / C;
+  const int64_t cbase = chunk_offsets ? chunk_offsets[n] : n * ((T + C - 1) / C);
+
+  for (int64_t e = tid; e < K * kBVh; e += kThreads) {
+    const int64_t d = e / kBVh, vv = e % kBVh;
+    hs[e] = (h0 && v0 + vv < V) ? h0[((n * HV + hv) * K + d) * V + v0 + vv] : 0.f;
+  }
+  __syncthreads();
+
+  for (int64_t c = 0; c < nch; ++c) {
+    const int64_t t0 = sr.bos + c * C;
+    const int Lc = (int)(sr.eos - t0 < (int64_t)C ? sr.eos - t0 : (int64_t)C);
+    if (h)
+      for (int64_t e = tid; e < K * kBVh; e += kThreads) {
+        const int64_t d = e / kBVh, vv = e % kBVh;
+        if (v0 + vv < V) h[(((cbase + c) * HV + hv) * K + d) * V + v0 + vv] = hs[e];
+      }
+    const int64_t tl = t0 + Lc - 1;  // last valid token of the chunk
+    for (int64_t d = tid; d < K; d += kThreads)
+      gl[d] = PER_K ? gcum[(tl * HV + hv) * K + d] : gcum[tl * HV + hv];
+    __syncthreads();
+    for (int i = warp; i < C; i += kWarps) {
+      load_row_normed(k, t0 + i, H, hq, K, i < Lc, l2, kt + i * K, lane);
+      for (int64_t d = lane; d < K; d += 32) {
+        const float gi = i < Lc ? (PER_K ? gcum[((t0 + i) * HV + hv) * K + d] : gcum[(t0 + i) * HV + hv]) : 0.f;
+        kt[i * K + d] *= (i < Lc) ? expf(gl[d] - gi) : 0.f;
+        ws[i * K + d] = i < Lc ? w[((t0 + i) * HV + hv) * K + d] : 0.f;
+      }
+    }
+    __syncthreads();
+    // v_new = u - w h
+    for (int64_t e = tid; e < C * kBVh; e += kThreads) {
+      const int i = (int)(e / kBVh), vv = (int)(e % kBVh);
+      float acc = 0.f;
+      if (i < Lc && v0 + vv < V) {
+        acc = u[((t0 + i) * HV + hv) * V + v0 + vv];
+        for (int64_t d = 0; d < K; ++d) acc = fmaf(-ws[i * K + d], hs[d * kBVh + vv], acc);
+        if (v_new) v_new[((t0 + i) * HV + hv) * V + v0 + vv] = acc;
+      }
+      vn[e] = acc;
+    }
+    __syncthreads();
+    // h <- exp(G_C) h + (K * exp(G_C - G))^T v_new
+    for (int64_t e = tid; e < K * kBVh; e += kThreads) {
+      const int64_t d = e / kBVh, vv = e % kBVh;
+      float acc = hs[e] * expf(gl[d]);
+      for (int i = 0; i < Lc; ++i) acc = fmaf(kt[i * K + d], vn[i * kBVh + vv], acc);
+      hs[e] = acc;
+    }
+    __syncthreads();
+  }
+  if (ht)
+    for (int64_t e = tid; e < K * kBVh; e += kThreads) {
+      const int64_t d = e / kBVh, vv = e % kBVh;
+      if (v0 + vv < V) ht[((n * HV + hv) * K + d) * V + v0 + vv] = hs[e];
+    }
+}
+
+// --------------------------------------------------------------------------
+// fwd_o: grid (nt_max, HV).  V is walked in tiles of C columns.
+// smem: qs[C*K] | ks[C*K] (reused for the h tile [K*C]) | gam[C*K or C] | P[C*C] | vn[C*C]
+// --------------------------------------------------------------------------
+template <typename Tin, int C, bool PER_K>
+__global__ void __launch_bounds__(kThreads) fwd_o_kernel(
+    const Tin *__restrict__ q, const Tin *__restrict__ k, const float *__restrict__ v_new,
+    const float *__restrict__ h, const float *__restrict__ gcum, const int64_t *__restrict__ cu,
+    const int64_t *__restrict__ chunk_indices, int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V,
+    int l2, Tin *__restrict__ o) {
+  extern __shared__ float smem[];
+  float *qs = smem;
+  float *ks = qs + C * K;
+  float *hs = ks;
+  float *gam = ks + C * K;
+  float *P = gam + (PER_K ? C * K : C);
+  float *vn = P + C * C;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t chunk = blockIdx.x, hv = blockIdx.y;
+  int64_t n, j;
+  if (!chunk_coords(chunk_indices, chunk, T, C, &n, &j)) return;
+  const SeqRange sr = seq_range(cu, n, T);
+  const int64_t t0 = sr.bos + j * C;
+  const int Lc = (int)(sr.eos - t0 < (int64_t)C ? sr.eos - t0 : (int64_t)C);
+  const int64_t hq = hv / (HV / H);
+
+  for (int i = warp; i < C; i += kWarps) {
+    load_row_normed(q, t0 + i, H, hq, K, i < Lc, l2, qs + i * K, lane);
+    load_row_normed(k, t0 + i, H, hq, K, i < Lc, l2, ks + i * K, lane);
+  }
+  if (PER_K) {
+    for (int64_t e = tid; e < C * K; e += kThreads) {
+      const int64_t i = e / K, d = e % K;
+      gam[e] = i < Lc ? gcum[((t0 + i) * HV + hv) * K + d] : 0.f;
+    }
+  } else {
+    for (int i = tid; i < C; i += kThreads) gam[i] = i < Lc ? gcum[(t0 + i) * HV + hv] : 0.f;
+  }
+  __syncthreads();
+  // P_ri = sum_d q_rd k_id exp(G_rd - G_id), i <= r
+  for (int p = warp; p < C * C; p += kWarps) {
+    const int r = p / C, i = p % C;
+    if (i > r || r >= Lc) {
+      if (lane == 0) P[p] = 0.f;
+      continue;
+    }
+    float s = 0.f;
+    for (int64_t d = lane; d < K; d += 32) {
+      float t = qs[r * K + d] * ks[i * K + d];
+      if (PER_K) t *= expf(gam[r * K + d] - gam[i * K + d]);
+      s += t;
+    }
+    s = warp_sum(s);
+    if (lane == 0) P[p] = s * (PER_K ? 1.f : expf(gam[r] - gam[i]));
+  }
+  __syncthreads();
+  for (int64_t e = tid; e < C * K; e += kThreads) qs[e] *= expf(PER_K ? gam[e] : gam[e / K]);
+  __syncthreads();
+
+  for (int64_t v0 = 0; v0 < V; v0 += C) {
+    for (int64_t e = tid; e < K * C; e += kThreads) {
+      const int64_t d = e / C, vv = e % C;
+      hs[e] = v0 + vv < V ? h[((chunk * HV + hv) * K + d) * V + v0 + vv] : 0.f;
+    }
+    for (int64_t e = tid; e < C * C; e += kThreads) {
+      const int64_t i = e / C, vv = e % C;
+      vn[e] = (i < Lc && v0 + vv < V) ? v_new[((t0 + i) * HV + hv) * V + v0 + vv] : 0.f;
+    }
+    __syncthreads();
+    for (int64_t e = tid; e < C * C; e += kThreads) {
+      const int r = (int)(e / C), vv = (int)(e % C);
+      if (r < Lc && v0 + vv < V) {
+        float acc = 0.f;
+        for (int64_t d = 0; d < K; ++d) acc = fmaf(qs[r * K + d], hs[d * C + vv], acc);
+        for (int i = 0; i <= r; ++i) acc = fmaf(P[r * C + i], vn[i * C + vv], acc);
+        o[((t0 + r) * HV + hv) * V + v0 + vv] = from_f32<Tin>(acc);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+template <typename F>
+int launch_checked(F kernel, dim3 grid, size_t smem, cudaStream_t s, const char *name) {
+  (void)s;
+  if (grid.x == 0 || grid.y == 0 || grid.z == 0) return GDR_OK;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return cuda_error(e, name);
+  return GDR_OK;
+}
+
+int check_launch(const char *name) {
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? GDR_OK : cuda_error(e, name);
+}
+
+}  // namespace
+
+int launch_chunk_index(const ChunkedArgs &a) {
+  chunk_index_kernel<<<1, kThreads, 0, a.stream>>>(a.cu, a.d.N, a.d.T, a.C, a.nt_max, a.chunk_indices,
+                                                   a.chunk_offsets, a.status);
+  return check_launch("chunk_index_kernel");
+}
+
+template <int C_, bool PK_>
+struct Cfg {
+  static constexpr int C = C_;
+  static constexpr bool PK = PK_;
+};
+
+// Calls f(Cfg<C, per_k>{}) for the runtime chunk size and gate kind.
+template <typename F>
+int dispatch_cfg(int C, bool per_k, F &&f) {
+  if (C == 64) return per_k ? f(Cfg<64, true>{}) : f(Cfg<64, false>{});
+  return per_k ? f(Cfg<32, true>{}) : f(Cfg<32, false>{});
+}
+
+template <typename Tin>
+static int prepare_t(const ChunkedArgs &a) {
+  const int64_t K = a.d.K, V = a.d.V;
+  return dispatch_cfg(a.C, a.d.gate == GDR_GATE_PER_K, [&](auto cfg) {
+    constexpr int CC = decltype(cfg)::C;
+    constexpr bool PK = decltype(cfg)::PK;
+    const size_t smem = sizeof(float) * (CC * K + (PK ? CC * K : CC) + CC + CC * CC);
+    auto kern = prepare_kernel<Tin, CC, PK>;
+    dim3 grid((unsigned)a.nt_max, (unsigned)a.d.HV);
+    int rc = launch_checked(kern, grid, smem, a.stream, "prepare_kernel");
+    if (rc == GDR_OK && a.nt_max > 0) {
+      kern<<<grid, kThreads, smem, a.stream>>>((const Tin *)a.k, (const Tin *)a.v, a.g, (const Tin *)a.beta, a.cu,
+                                               a.chunk_indices, a.d.T, a.d.H, a.d.HV, K, V, a.l2, a.gcum, a.w,
+                                               a.u);
+      rc = check_launch("prepare_kernel");
+    }
+    return rc;
+  });
+}
+
+template <typename Tin>
+static int fwd_h_t(const ChunkedArgs &a) {
+  const int64_t K = a.d.K, V = a.d.V;
+  return dispatch_cfg(a.C, a.d.gate == GDR_GATE_PER_K, [&](auto cfg) {
+    constexpr int CC = decltype(cfg)::C;
+    constexpr bool PK = decltype(cfg)::PK;
+    const size_t smem = sizeof(float) * (K * kBVh + 2 * CC * K + CC * kBVh + K);
+    auto kern = fwd_h_kernel<Tin, CC, PK>;
+    dim3 grid((unsigned)a.d.N, (unsigned)a.d.HV, (unsigned)cdiv(V, kBVh));
+    int rc = launch_checked(kern, grid, smem, a.stream, "fwd_h_kernel");
+    if (rc == GDR_OK && a.d.N > 0) {
+      kern<<<grid, kThreads, smem, a.stream>>>((const Tin *)a.k, a.w, a.u, a.gcum, a.h0, a.cu, a.chunk_offsets,
+                                               a.d.N, a.d.T, a.d.H, a.d.HV, K, V, a.l2, a.h, a.v_new, a.ht);
+      rc = check_launch("fwd_h_kernel");
+    }
+    return rc;
+  });
+}
+
+template <typename Tin>
+static int fwd_o_t(const ChunkedArgs &a) {
+  const int64_t K = a.d.K, V = a.d.V;
+  return dispatch_cfg(a.C, a.d.gate == GDR_GATE_PER_K, [&](auto cfg) {
+    constexpr int CC = decltype(cfg)::C;
+    constexpr bool PK = decltype(cfg)::PK;
+    const size_t smem = sizeof(float) * (2 * CC * K + (PK ? CC * K : CC) + 2 * CC * CC);
+    auto kern = fwd_o_kernel<Tin, CC, PK>;
+    dim3 grid((unsigned)a.nt_max, (unsigned)a.d.HV);
+    int rc = launch_checked(kern, grid, smem, a.stream, "fwd_o_kernel");
+    if (rc == GDR_OK && a.nt_max > 0) {
+      kern<<<grid, kThreads, smem, a.stream>>>((const Tin *)a.q, (const Tin *)a.k, a.v_new, a.h, a.gcum, a.cu,
+                                               a.chunk_indices, a.d.T, a.d.H, a.d.HV, K, V, a.l2, (Tin *)a.o);
+      rc = check_launch("fwd_o_kernel");
+    }
+    return rc;
+  });
+}
+
+int launch_chunk_prepare(const ChunkedArgs &a) {
+  return a.d.dtype == GDR_BF16 ? prepare_t<__nv_bfloat16>(a) : prepare_t<float>(a);
+}
+int launch_chunk_fwd_h(const ChunkedArgs &a) {
+  return a.d.dtype == GDR_BF16 ? fwd_h_t<__nv_bfloat16>(a) : fwd_h_t<float>(a);
+}
+int launch_chunk_fwd_o(const ChunkedArgs &a) {
+  return a.d.dtype == GDR_BF16 ? fwd_o_t<__nv_bfloat16>(a) : fwd_o_t<float>(a);
+}
+
+}  // namespace gdr

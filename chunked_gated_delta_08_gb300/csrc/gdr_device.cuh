@@ -1,0 +1,42 @@
+// gdr_device.cuh -- small device helpers shared by the kernels of libgdr.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace gdr {
+
+// Element conversions for the two input dtypes.
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// L2-norm reading: x / sqrt(sum x^2 + 1e-6), per token and head.
+constexpr float kL2Eps = 1e-6f;
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Token range [bos, eos) of sequence n: the varlen layout reads cu_seqlens,
+// the dense layout is n*T .. (n+1)*T.  int64 throughout.
+struct SeqRange {
+  int64_t bos, eos;
+};
+__device__ __forceinline__ SeqRange seq_range(const int64_t *cu, int64_t n, int64_t T) {
+  if (cu) return {cu[n], cu[n + 1]};
+  return {n * T, (n + 1) * T};
+}
+
+// Records the first problem seen by any kernel into the status word.
+__device__ __forceinline__ void raise_status(int *status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+}  // namespace gdr

@@ -1,0 +1,54 @@
+// gdr_internal.h -- declarations shared by the translation units of libgdr.so.
+// Host-side only; device helpers live in gdr_device.cuh.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "gdr.h"
+
+namespace gdr {
+
+// Records a message for gdr_last_error() on this thread and returns `code`.
+int set_error(int code, const std::string &msg);
+int cuda_error(cudaError_t e, const char *what);
+
+// Counts kernel launches (gdr_launch_count).
+void count_launch(int n = 1);
+
+// Per-device 4-byte status word that kernels set on a detected problem
+// (bad cu_seqlens, an expired bounded wait).  Zero means OK.
+int *device_status_word(int device, int *err);
+
+// Geometry shared by the launchers: number of chunks in the dense layout,
+// and an upper bound on NT for the varlen layout.
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t nt_upper_bound(const gdr_desc &d, int C) {
+  // sum_n ceil(len_n / C) <= (T + N (C - 1)) / C when the lengths sum to T
+  return d.N > 0 ? (d.B * d.T + d.N * (int64_t)(C - 1)) / C : 0;
+}
+
+struct ChunkedArgs {
+  gdr_desc d;
+  int C;
+  int l2;
+  const void *q, *k, *v, *beta;
+  const float *g, *h0;
+  const int64_t *cu;
+  int64_t *chunk_indices, *chunk_offsets;  // may be null in the dense layout
+  float *gcum, *w, *u, *h, *v_new, *ht;
+  void *o;
+  int64_t nt_max;
+  int *status;
+  cudaStream_t stream;
+};
+
+// Launchers of the chunked (three-kernel) form; return GDR_OK or an error.
+int launch_chunk_index(const ChunkedArgs &a);
+int launch_chunk_prepare(const ChunkedArgs &a);
+int launch_chunk_fwd_h(const ChunkedArgs &a);
+int launch_chunk_fwd_o(const ChunkedArgs &a);
+
+}  // namespace gdr

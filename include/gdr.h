@@ -1,0 +1,163 @@
+/*
+ * gdr.h -- C ABI of the GB300 (sm_103a) chunked gated delta rule forward.
+ *
+ * The operation (the gated delta rule, GDN with a scalar gate, KDA with a
+ * per-key-channel gate), per sequence and value head, with S a K x V state:
+ *
+ *   S_t = (I - beta_t k_t k_t^T) Diag(exp g_t) S_{t-1} + beta_t k_t v_t^T
+ *   o_t = S_t^T q_t
+ *
+ * evaluated chunk by chunk through the WY / UT-transform form
+ * S^r = P^r S^0 + H^r, P^r = I - sum_i k^i w^i^T ("FLA 算子内核正确性测试与覆盖矩阵",
+ * section 二), with the per-chunk state h stored at each chunk's START
+ * ("flash-linear-attention KCP 精度失效根因排查手册", section on h/dh semantics).
+ * The kernel order is the pages' forward order: chunk index -> prepare
+ * (L2 norm, gate cumsum, A, triangular solve, w, u) -> state scan (fwd_h)
+ * -> output (fwd_o) (KCP handbook, section on the debug-script layout).
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers to contiguous row-major memory,
+ *    owned by the caller; the library never frees or retains them.
+ *  - Shapes travel in a gdr_desc.  Token index t runs over B*T flat tokens.
+ *      q, k        [B, T, H, K]      dtype (fp32 or bf16)
+ *      v, o        [B, T, HV, V]     dtype
+ *      g           [B, T, HV] (GDN) or [B, T, HV, K] (KDA), fp32, natural-log decay
+ *      beta        [B, T, HV]        dtype (already in (0, 1); no sigmoid is applied)
+ *      h0, ht      [N, HV, K, V]     fp32, nullable
+ *      cu_seqlens  [N + 1]           int64, nullable; requires B == 1
+ *    Value head hv reads q/k head hv / (HV / H) (grouped value heads, GVA).
+ *  - q is not scaled (scale 1).  o has the dtype of q, k, v.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL
+ *    is the legacy default stream) and never synchronize the host, except
+ *    gdr_device_status.
+ *  - Every entry point returns GDR_OK (0) or a negative gdr_status.  On error
+ *    nothing has been launched and gdr_last_error() holds a message for the
+ *    calling thread.
+ *  - The current CUDA device must be the one that owns the pointers.
+ */
+#ifndef GDR_H
+#define GDR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdr_status {
+  GDR_OK = 0,
+  GDR_ERR_CHUNK_SIZE = -1,  /* chunk_size not in {32, 64}: "chunk_size must be either 32 or 64" */
+  GDR_ERR_SHAPE = -2,       /* bad sizes: HV % H != 0, K or V outside [1, 256], B != 1 with cu_seqlens, ... */
+  GDR_ERR_DTYPE = -3,       /* unknown dtype / gate / algorithm code */
+  GDR_ERR_NULLPTR = -4,     /* a required pointer is NULL */
+  GDR_ERR_ALIGN = -5,       /* a pointer the fused path stages with TMA is not 16-byte aligned */
+  GDR_ERR_CUDA = -6,        /* a CUDA runtime call failed (message has the CUDA error string) */
+  GDR_ERR_TIMEOUT = -7,     /* a bounded device-side wait expired (reported by gdr_device_status) */
+  GDR_ERR_SEQLENS = -8,     /* cu_seqlens not monotone or not spanning [0, T] (gdr_device_status) */
+  GDR_ERR_UNSUPPORTED = -9  /* valid request that the chosen algorithm does not implement */
+} gdr_status;
+
+typedef enum gdr_dtype { GDR_F32 = 0, GDR_BF16 = 1 } gdr_dtype;
+typedef enum gdr_gate { GDR_GATE_SCALAR = 0, GDR_GATE_PER_K = 1 } gdr_gate;
+typedef enum gdr_algo {
+  GDR_ALGO_AUTO = 0,     /* fused single pass where supported, else the chunked three-kernel form */
+  GDR_ALGO_CHUNKED = 1,  /* chunk index -> prepare -> fwd_h -> fwd_o, fp32 CUDA-core arithmetic */
+  GDR_ALGO_FUSED = 2     /* one persistent pass per (sequence, value head), tcgen05 tensor cores */
+} gdr_algo;
+
+typedef struct gdr_desc {
+  int64_t B, T, H, HV, K, V;
+  int64_t N;       /* number of sequences: B when cu_seqlens is NULL, else len(cu_seqlens) - 1 */
+  int32_t dtype;   /* gdr_dtype of q, k, v, beta, o */
+  int32_t gate;    /* gdr_gate */
+  int32_t algo;    /* gdr_algo */
+  int32_t flags;   /* reserved, must be 0 */
+} gdr_desc;
+
+/*
+ * gdr_fwd -- the chunked forward of the gated delta rule.
+ *   chunk_size     32 or 64; anything else returns GDR_ERR_CHUNK_SIZE (the
+ *                  coverage guide, section 三, rejects chunk_size = 16 this way).
+ *   use_qk_l2norm  nonzero: q and k are L2-normalized per token and head inside
+ *                  the kernels, x / sqrt(sum x^2 + 1e-6); zero: used as given.
+ *   h0             initial state, NULL means zero.
+ *   ht             final state output, NULL means not wanted.
+ *   cu_seqlens     NULL for dense batches; else the varlen layout.  Its values
+ *                  are read on the device: they must be non-decreasing with
+ *                  cu[0] = 0 and cu[N] = T; a violation makes every output
+ *                  untouched and is reported by gdr_device_status.
+ * Scratch (the chunked form's w, u, h, v_new) is taken stream-ordered from a
+ * library-owned memory pool on `stream` and returned to it before the call's
+ * work completes; the fused form needs none.
+ */
+int gdr_fwd(const gdr_desc *desc, const void *q, const void *k, const void *v, const float *g,
+            const void *beta, const float *h0, const int64_t *cu_seqlens, int chunk_size,
+            int use_qk_l2norm, void *o, float *ht, void *stream);
+
+/*
+ * Stage entry points of the chunked form, with caller-provided scratch, so the
+ * per-chunk intermediates can be inspected.  Sizes come from gdr_chunked_sizes.
+ *
+ *   gdr_chunk_index    cu_seqlens [N+1] -> chunk_indices [nt_max, 2] (sequence,
+ *                      chunk-in-sequence), chunk_offsets [N+1] (first chunk of
+ *                      each sequence; chunk_offsets[N] = NT).  Rows >= NT of
+ *                      chunk_indices are set to -1.  int64 throughout
+ *                      (coverage guide, section 四: address arithmetic in int64).
+ *                      With cu_seqlens NULL it describes the dense layout.
+ *   gdr_chunk_prepare  per (chunk, value head): gate cumsum Gamma (fp32, [B*T, HV]
+ *                      or [B*T, HV, K]), A = tril(beta K K^T * decay, -1),
+ *                      T = (I + A)^-1, w = T diag(beta) (K * exp Gamma)
+ *                      ([B*T, HV, K] fp32) and u = T diag(beta) V ([B*T, HV, V] fp32).
+ *   gdr_chunk_fwd_h    per (sequence, value head, V-tile), sequential over
+ *                      chunks: h [NT, HV, K, V] fp32 (state entering each chunk),
+ *                      v_new = u - w h ([B*T, HV, V] fp32), and ht.
+ *   gdr_chunk_fwd_o    per (chunk, value head): o = (q * exp Gamma) h +
+ *                      tril(q k^T * decay) v_new.
+ */
+typedef struct gdr_chunked_sizes {
+  int64_t nt_max;              /* upper bound on the number of chunks NT */
+  size_t chunk_indices_bytes;  /* int64 [nt_max, 2] */
+  size_t chunk_offsets_bytes;  /* int64 [N + 1] */
+  size_t gcum_bytes;           /* fp32 gate cumsum */
+  size_t w_bytes, u_bytes, v_new_bytes, h_bytes;
+} gdr_chunked_sizes;
+
+/* varlen nonzero: sizes for the cu_seqlens layout (nt_max is then an upper bound). */
+int gdr_chunked_sizes_get(const gdr_desc *desc, int chunk_size, int varlen, gdr_chunked_sizes *out);
+int gdr_chunk_index(const gdr_desc *desc, const int64_t *cu_seqlens, int chunk_size,
+                    int64_t *chunk_indices, int64_t *chunk_offsets, void *stream);
+int gdr_chunk_prepare(const gdr_desc *desc, const void *k, const void *v, const float *g,
+                      const void *beta, const int64_t *cu_seqlens, const int64_t *chunk_indices,
+                      int chunk_size, int use_qk_l2norm, float *gcum, float *w, float *u, void *stream);
+int gdr_chunk_fwd_h(const gdr_desc *desc, const void *k, const float *w, const float *u,
+                    const float *gcum, const float *h0, const int64_t *cu_seqlens,
+                    const int64_t *chunk_offsets, int chunk_size, int use_qk_l2norm, float *h,
+                    float *v_new, float *ht, void *stream);
+int gdr_chunk_fwd_o(const gdr_desc *desc, const void *q, const void *k, const float *v_new,
+                    const float *h, const float *gcum, const int64_t *cu_seqlens,
+                    const int64_t *chunk_indices, int chunk_size, int use_qk_l2norm, void *o,
+                    void *stream);
+
+/*
+ * gdr_device_status -- synchronizes `stream`, then returns (and, if `clear`,
+ * resets) the library's device-side status word for the current device:
+ * GDR_OK, GDR_ERR_SEQLENS or GDR_ERR_TIMEOUT.  Also returns GDR_ERR_CUDA if
+ * the stream itself reports an error.
+ */
+int gdr_device_status(void *stream, int clear);
+
+/* Message for the last error on the calling thread ("" if none). */
+const char *gdr_last_error(void);
+
+/* Number of kernels this library has launched in this process (all devices). */
+int64_t gdr_launch_count(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int gdr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDR_H */

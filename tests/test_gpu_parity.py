@@ -1,0 +1,261 @@
+"""CUDA path (through the C ABI) against the fp64 oracle, element by element.
+
+Tolerances: relative L2 error <= 1e-5 for fp32 inputs and <= 5e-3 for bf16
+inputs, on o and ht (the 0.005 assert_close bar of the coverage guide,
+section 三; the fp32 bar is the tighter one set for fp32 inputs).  The metric is
+||x - ref||_2 / ||ref||_2 over the whole tensor (FLA contributor guide,
+section Testing: RMS(diff) / RMS(ref)), with any NaN a failure.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 1e-5, torch.bfloat16: 5e-3}
+ALGOS = ["chunked", "auto"]
+
+
+@pytest.fixture(scope="module")
+def gdr():
+    from chunked_gated_delta_08_gb300 import _build
+    _build.build()
+    import chunked_gated_delta_08_gb300 as m
+    return m
+
+
+def rel_l2(got, want):
+    got = got.detach().double().cpu().numpy() if hasattr(got, "detach") else np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    assert np.isfinite(got).all(), "non-finite values in the CUDA output"
+    den = np.linalg.norm(want)
+    return float(np.linalg.norm(got - want) / (den if den > 0 else 1.0))
+
+
+def to_dev(x):
+    return {k: (None if v is None else v.cuda()) for k, v in x.items()}
+
+
+def poisoned_like(shape, dtype):
+    return torch.full(shape, float("nan"), dtype=dtype, device="cuda")
+
+
+def run_gpu(gdr, x, C, l2, algo, poison=True):
+    d = to_dev(x)
+    B, T, H, K = d["q"].shape
+    HV, V = d["v"].shape[2], d["v"].shape[3]
+    N = B if d["cu_seqlens"] is None else d["cu_seqlens"].numel() - 1
+    o = poisoned_like((B, T, HV, V), d["q"].dtype) if poison else None
+    ht = poisoned_like((N, HV, K, V), torch.float32) if poison else None
+    o, ht = gdr.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0=d["h0"], cu_seqlens=d["cu_seqlens"],
+                    chunk_size=C, use_qk_l2norm=l2, algo=algo, out=o, final_state=ht)
+    assert gdr.device_status() == 0, gdr.last_error()
+    return o, ht
+
+
+def run_ref(x, l2, **kw):
+    return oracle.gdr_fwd_ref(x["q"], x["k"], x["v"], x["g"], x["beta"], h0=x["h0"], cu_seqlens=x["cu_seqlens"],
+                              use_qk_l2norm=l2, **kw)
+
+
+def assert_parity(o, ht, ref, dtype, what=""):
+    tol = TOL[dtype]
+    eo, eh = rel_l2(o, ref["o"]), rel_l2(ht, ref["ht"])
+    assert eo <= tol and eh <= tol, f"{what}: o err {eo:.2e}, ht err {eh:.2e} (tol {tol:.0e})"
+    return eo, eh
+
+
+# ---------------------------------------------------------------- the five workloads
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("w", [wl.GDN_FP32_SMALL, wl.GDN_BF16_GVA_K60, wl.GDN_BF16_VARLEN, wl.KDA_BF16_VARLEN],
+                         ids=lambda w: w.name)
+def test_workload_parity(gdr, w, algo):
+    x = wl.make_inputs(w)
+    o, ht = run_gpu(gdr, x, w.chunk_size, w.use_qk_l2norm, algo)
+    ref = run_ref(x, w.use_qk_l2norm)
+    assert_parity(o, ht, ref, w.dtype, w.name)
+
+
+def test_gva_workload_rejects_chunk_size_16(gdr):
+    w = wl.GDN_BF16_GVA_K60
+    d = to_dev(wl.make_inputs(w))
+    with pytest.raises(ValueError, match="chunk_size must be either 32 or 64"):
+        gdr.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0=d["h0"], chunk_size=16, use_qk_l2norm=True)
+
+
+def test_varlen_equals_separate_runs_bitwise(gdr):
+    """Sequences of a varlen batch give exactly the bits they give alone."""
+    w = wl.GDN_BF16_VARLEN
+    x = wl.make_inputs(w)
+    for algo in ALGOS:
+        o, ht = run_gpu(gdr, x, w.chunk_size, w.use_qk_l2norm, algo)
+        cu = w.cu_seqlens
+        for n in range(w.N):
+            s0, s1 = cu[n], cu[n + 1]
+            part = {"q": x["q"][:, s0:s1].contiguous(), "k": x["k"][:, s0:s1].contiguous(),
+                    "v": x["v"][:, s0:s1].contiguous(), "g": x["g"][:, s0:s1].contiguous(),
+                    "beta": x["beta"][:, s0:s1].contiguous(), "h0": x["h0"][n:n + 1].contiguous(),
+                    "cu_seqlens": None}
+            op, hp = run_gpu(gdr, part, w.chunk_size, w.use_qk_l2norm, algo)
+            assert torch.equal(op, o[:, s0:s1]), f"{algo}: o of sequence {n} differs from its separate run"
+            assert torch.equal(hp[0], ht[n]), f"{algo}: ht of sequence {n} differs from its separate run"
+
+
+# ---------------------------------------------------------------- large dense workload, sampled
+@pytest.mark.parametrize("algo", ALGOS)
+def test_large_dense_sampled_units(gdr, algo):
+    """Full-size B=4, T=32768, H=HV=32, K=V=128 bf16 run; the oracle checks sampled
+    (sequence, head) units whole, and every output is finite."""
+    w = wl.GDN_BF16_LARGE
+    x = wl.make_inputs(w)
+    o, ht = run_gpu(gdr, x, w.chunk_size, w.use_qk_l2norm, algo)
+    assert torch.isfinite(o).all() and torch.isfinite(ht).all()
+    units = [(0, 0), (3, 31), (1, 17), (2, 5)]
+    ref = oracle.gdr_fwd_ref_units(x["q"], x["k"], x["v"], x["g"], x["beta"], units, use_qk_l2norm=True)
+    for (n, hv), (ro, rh) in ref.items():
+        eo = rel_l2(o[n, :, hv], ro)
+        eh = rel_l2(ht[n, hv], rh)
+        assert eo <= TOL[w.dtype] and eh <= TOL[w.dtype], f"unit {(n, hv)}: o {eo:.2e} ht {eh:.2e}"
+
+
+# ---------------------------------------------------------------- unit grid
+GRID = [
+    # B, T, H, HV, K, V, lengths, per_k
+    (1, 1, 1, 1, 64, 64, None, False),
+    (1, 63, 1, 1, 64, 64, None, False),
+    (2, 64, 1, 2, 64, 32, None, False),
+    (1, 65, 2, 2, 60, 60, None, False),
+    (2, 100, 2, 4, 60, 100, None, False),
+    (1, 2000, 1, 1, 128, 128, None, False),
+    (1, 300, 1, 3, 32, 48, (1, 64, 0, 170, 65), False),
+    (1, 64, 1, 1, 64, 64, None, True),
+    (1, 64, 1, 2, 64, 64, None, True),
+    (2, 512, 2, 4, 60, 60, None, True),
+    (1, 333, 2, 4, 128, 256, (100, 233), True),
+]
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("C", [32, 64])
+@pytest.mark.parametrize("case", GRID, ids=lambda c: "x".join(str(v) for v in c[:6]) + ("_kda" if c[7] else ""))
+def test_unit_grid(gdr, case, C, dtype, algo):
+    B, T, H, HV, K, V, lengths, per_k = case
+    for l2, use_h0 in ((True, True), (False, False)):
+        _, x = wl.random_case(B, T, H, HV, K, V, dtype=dtype, lengths=lengths, gate_per_k=per_k,
+                              use_h0=use_h0, seed=T + K)
+        o, ht = run_gpu(gdr, x, C, l2, algo)
+        ref = run_ref(x, l2)
+        assert_parity(o, ht, ref, dtype, f"{case} C={C} l2={l2} h0={use_h0}")
+
+
+# ---------------------------------------------------------------- over-read detection
+@pytest.mark.parametrize("per_k", [False, True])
+def test_padding_poison_detects_overreads(gdr, per_k):
+    """Inputs sit at the front of buffers whose tails hold NaN (q, k, v, beta) or
+    1e30 (g, the coverage guide's section 七 padding); any read past a tensor's
+    end would make the outputs non-finite or wrong."""
+    _, x = wl.random_case(1, 190, 1, 2, 60, 60, dtype=torch.bfloat16, gate_per_k=per_k, seed=5)
+    d = {}
+    for name in ("q", "k", "v", "beta", "g"):
+        t = x[name]
+        pad = 1e30 if name == "g" else float("nan")
+        buf = torch.full((t.numel() + 4096,), pad, dtype=t.dtype, device="cuda")
+        buf[:t.numel()].copy_(t.reshape(-1))
+        d[name] = buf[:t.numel()].view(t.shape)
+    h0 = x["h0"].cuda()
+    o, ht = gdr.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0=h0, chunk_size=64, use_qk_l2norm=True,
+                    out=poisoned_like((1, 190, 2, 60), torch.bfloat16),
+                    final_state=poisoned_like((1, 2, 60, 60), torch.float32))
+    ref = run_ref(x, True)
+    assert_parity(o, ht, ref, torch.bfloat16, "padded inputs")
+
+
+# ---------------------------------------------------------------- intermediates
+@pytest.mark.parametrize("per_k", [False, True])
+def test_chunk_intermediates(gdr, per_k):
+    """h (state entering each chunk) and the per-token v_new against the oracle's
+    per-token recurrence; w and u against the oracle's chunk-form helper."""
+    lengths = (70, 130)
+    _, x = wl.random_case(1, 200, 1, 2, 32, 24, dtype=torch.float32, lengths=lengths, gate_per_k=per_k, seed=9)
+    C = 32
+    st = gdr.chunk_stages(*[x[k].cuda() for k in ("q", "k", "v", "g", "beta")], h0=x["h0"].cuda(),
+                          cu_seqlens=x["cu_seqlens"].cuda(), chunk_size=C, use_qk_l2norm=True)
+    torch.cuda.synchronize()
+    ref = run_ref(x, True, chunk_size=C, want_v_new=True)
+    idx, off = oracle.chunk_index_ref(x["cu_seqlens"].numpy(), C)
+    NT = len(idx)
+    assert st["chunk_offsets"].cpu().tolist() == off.tolist()
+    assert st["chunk_indices"][:NT].cpu().tolist() == idx.tolist()
+    assert (st["chunk_indices"][NT:] == -1).all()
+    assert rel_l2(st["h"][:NT], ref["h_chunks"]) <= 1e-5
+    assert rel_l2(st["v_new"], ref["v_new"]) <= 1e-5
+    assert rel_l2(st["o"], ref["o"]) <= 1e-5 and rel_l2(st["ht"], ref["ht"]) <= 1e-5
+    cu = x["cu_seqlens"].tolist()
+    for (n, j) in idx[:: max(1, NT // 4)]:
+        s0 = cu[n] + j * C
+        s1 = min(s0 + C, cu[n + 1])
+        cf = oracle.chunk_form_ref(x["k"][0, s0:s1, 0].numpy(), x["v"][0, s0:s1, 1].numpy(),
+                                   x["g"][0, s0:s1, 1].numpy(), x["beta"][0, s0:s1, 1].numpy(),
+                                   use_qk_l2norm=True, gate_per_k=per_k)
+        assert rel_l2(st["w"][0, s0:s1, 1], cf["w"]) <= 1e-5
+        assert rel_l2(st["u"][0, s0:s1, 1], cf["u"]) <= 1e-5
+        gam = cf["Gamma"] if per_k else cf["Gamma"][:, 0]
+        assert rel_l2(st["gcum"][0, s0:s1, 1], gam) <= 1e-6
+
+
+# ---------------------------------------------------------------- semantics
+def test_resume_from_final_state(gdr):
+    _, x = wl.random_case(2, 300, 1, 2, 64, 64, dtype=torch.float32, seed=3)
+    d = to_dev(x)
+    o, ht = gdr.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0=d["h0"], chunk_size=64)
+    t1 = 131
+    sl = lambda t, a, b: t[:, a:b].contiguous()
+    o1, h1 = gdr.fwd(*[sl(d[k], 0, t1) for k in ("q", "k", "v", "g", "beta")], h0=d["h0"], chunk_size=64)
+    o2, h2 = gdr.fwd(*[sl(d[k], t1, 300) for k in ("q", "k", "v", "g", "beta")], h0=h1, chunk_size=64)
+    assert rel_l2(torch.cat([o1, o2], 1), o.double().cpu().numpy()) <= 1e-5
+    assert rel_l2(h2, ht.double().cpu().numpy()) <= 1e-5
+
+
+def test_no_final_state_and_zero_length(gdr):
+    _, x = wl.random_case(1, 0, 1, 1, 64, 64, dtype=torch.bfloat16, seed=1)
+    d = to_dev(x)
+    o, ht = gdr.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0=d["h0"], chunk_size=64)
+    assert o.numel() == 0 and torch.equal(ht, d["h0"])
+    _, x = wl.random_case(1, 70, 1, 1, 64, 64, dtype=torch.bfloat16, seed=1)
+    d = to_dev(x)
+    o, ht = gdr.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], chunk_size=64, output_final_state=False)
+    assert ht is None and torch.isfinite(o).all()
+
+
+def test_bad_cu_seqlens_reported_on_device(gdr):
+    _, x = wl.random_case(1, 100, 1, 1, 64, 64, dtype=torch.bfloat16, lengths=(40, 60), seed=2)
+    d = to_dev(x)
+    d["cu_seqlens"] = torch.tensor([0, 70, 60], dtype=torch.int64, device="cuda")
+    o = poisoned_like((1, 100, 1, 64), torch.bfloat16)
+    gdr.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], cu_seqlens=d["cu_seqlens"], chunk_size=64, out=o,
+            algo="chunked")
+    assert gdr.device_status(clear=True) == gdr.GDR_ERR_SEQLENS
+    assert torch.isnan(o.float()).all()
+    assert gdr.device_status() == 0
+
+
+def test_deterministic(gdr):
+    w = wl.GDN_BF16_GVA_K60
+    x = wl.make_inputs(w)
+    a = run_gpu(gdr, x, 64, True, "auto")
+    b = run_gpu(gdr, x, 64, True, "auto")
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_host_buffers_end_to_end(gdr):
+    w = wl.GDN_BF16_VARLEN
+    x = wl.make_inputs(w)
+    pinned = {k: (None if v is None else v.pin_memory()) for k, v in x.items()}
+    o_h, ht_h = gdr.fwd_host(pinned["q"], pinned["k"], pinned["v"], pinned["g"], pinned["beta"], h0=pinned["h0"],
+                             cu_seqlens=pinned["cu_seqlens"], chunk_size=64)
+    o_d, ht_d = run_gpu(gdr, x, 64, False, "auto", poison=False)
+    assert not o_h.is_cuda and torch.equal(o_h, o_d.cpu()) and torch.equal(ht_h, ht_d.cpu())
