@@ -90,7 +90,7 @@ def test_varlen_equals_separate_runs_bitwise(gdr):
     """Sequences of a varlen batch give exactly the bits they give alone."""
     w = wl.GDN_BF16_VARLEN
     x = wl.make_inputs(w)
-    for algo in ALGOS:
+    for algo in ["chunked", "fused"]:
         o, ht = run_gpu(gdr, x, w.chunk_size, w.use_qk_l2norm, algo)
         cu = w.cu_seqlens
         for n in range(w.N):
@@ -105,7 +105,7 @@ def test_varlen_equals_separate_runs_bitwise(gdr):
 
 
 # ---------------------------------------------------------------- large dense workload, sampled
-@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("algo", ["chunked", "fused"])
 def test_large_dense_sampled_units(gdr, algo):
     """Full-size B=4, T=32768, H=HV=32, K=V=128 bf16 run; the oracle checks sampled
     (sequence, head) units whole, and every output is finite."""
@@ -153,12 +153,12 @@ def test_unit_grid(gdr, case, C, dtype, algo):
 
 
 # ---------------------------------------------------------------- over-read detection
-@pytest.mark.parametrize("per_k", [False, True])
-def test_padding_poison_detects_overreads(gdr, per_k):
+@pytest.mark.parametrize("per_k,D", [(False, 60), (True, 60), (False, 128)])
+def test_padding_poison_detects_overreads(gdr, per_k, D):
     """Inputs sit at the front of buffers whose tails hold NaN (q, k, v, beta) or
     1e30 (g, the coverage guide's section 七 padding); any read past a tensor's
-    end would make the outputs non-finite or wrong."""
-    _, x = wl.random_case(1, 190, 1, 2, 60, 60, dtype=torch.bfloat16, gate_per_k=per_k, seed=5)
+    end would make the outputs non-finite or wrong.  D = 128 takes the fused form."""
+    _, x = wl.random_case(1, 190, 1, 2, D, D, dtype=torch.bfloat16, gate_per_k=per_k, seed=5)
     d = {}
     for name in ("q", "k", "v", "beta", "g"):
         t = x[name]
@@ -168,8 +168,8 @@ def test_padding_poison_detects_overreads(gdr, per_k):
         d[name] = buf[:t.numel()].view(t.shape)
     h0 = x["h0"].cuda()
     o, ht = gdr.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0=h0, chunk_size=64, use_qk_l2norm=True,
-                    out=poisoned_like((1, 190, 2, 60), torch.bfloat16),
-                    final_state=poisoned_like((1, 2, 60, 60), torch.float32))
+                    out=poisoned_like((1, 190, 2, D), torch.bfloat16),
+                    final_state=poisoned_like((1, 2, D, D), torch.float32))
     ref = run_ref(x, True)
     assert_parity(o, ht, ref, torch.bfloat16, "padded inputs")
 
@@ -259,3 +259,57 @@ def test_host_buffers_end_to_end(gdr):
                              cu_seqlens=pinned["cu_seqlens"], chunk_size=64)
     o_d, ht_d = run_gpu(gdr, x, 64, False, "auto", poison=False)
     assert not o_h.is_cuda and torch.equal(o_h, o_d.cpu()) and torch.equal(ht_h, ht_d.cpu())
+
+
+# ---------------------------------------------------------------- fused tensor-core form
+FUSED_GRID = [
+    # B, T, H, HV, lengths
+    (1, 64, 1, 1, None),
+    (2, 1000, 1, 2, None),
+    (1, 1, 1, 1, None),
+    (3, 130, 2, 4, None),
+    (1, 777, 1, 2, (1, 63, 64, 65, 584)),
+    (1, 2048, 4, 4, (0, 1024, 1024)),
+]
+
+
+@pytest.mark.parametrize("case", FUSED_GRID, ids=lambda c: "x".join(str(v) for v in c[:4]) + ("_varlen" if c[4] else ""))
+def test_fused_grid(gdr, case):
+    B, T, H, HV, lengths = case
+    for l2, use_h0 in ((True, True), (False, False)):
+        _, x = wl.random_case(B, T, H, HV, 128, 128, dtype=torch.bfloat16, lengths=lengths, use_h0=use_h0,
+                              seed=T + HV)
+        if not l2:
+            x["q"] = torch.nn.functional.normalize(x["q"].float(), dim=-1).to(torch.bfloat16)
+            x["k"] = torch.nn.functional.normalize(x["k"].float(), dim=-1).to(torch.bfloat16)
+        o, ht = run_gpu(gdr, x, 64, l2, "fused")
+        ref = run_ref(x, l2)
+        assert_parity(o, ht, ref, torch.bfloat16, f"fused {case} l2={l2} h0={use_h0}")
+
+
+def test_fused_matches_chunked_form(gdr):
+    """The two forms agree with each other as well as with the oracle."""
+    w = wl.GDN_BF16_VARLEN
+    x = wl.make_inputs(w)
+    of, hf = run_gpu(gdr, x, 64, False, "fused")
+    oc, hc = run_gpu(gdr, x, 64, False, "chunked")
+    assert rel_l2(of, oc.double().cpu().numpy()) <= 5e-3
+    assert rel_l2(hf, hc.double().cpu().numpy()) <= 5e-3
+
+
+@pytest.mark.parametrize("what", ["f32", "K60", "C32", "kda"])
+def test_fused_reports_unsupported(gdr, what):
+    kw = dict(B=1, T=70, H=1, HV=1, K=128, V=128, dtype=torch.bfloat16)
+    C = 64
+    if what == "f32":
+        kw["dtype"] = torch.float32
+    elif what == "K60":
+        kw["K"] = 60
+    elif what == "C32":
+        C = 32
+    _, x = wl.random_case(**kw, gate_per_k=(what == "kda"), seed=1)
+    with pytest.raises(gdr.GdrError) as ei:
+        run_gpu(gdr, x, C, True, "fused")
+    assert ei.value.code == gdr.GDR_ERR_UNSUPPORTED
+    o, ht = run_gpu(gdr, x, C, True, "auto")  # the dispatcher falls back to the chunked form
+    assert_parity(o, ht, run_ref(x, True), kw["dtype"], f"auto fallback {what}")
