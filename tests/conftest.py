@@ -20,3 +20,12 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def gdr():
+    """The built library's Python binding (builds libgdr.so first if needed)."""
+    import __graft_entry__
+    __graft_entry__.build_module().build()
+    import chunked_gated_delta_08_gb300 as m
+    return m

@@ -9,14 +9,6 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-@pytest.fixture(scope="module")
-def gdr():
-    from chunked_gated_delta_08_gb300 import _build
-    _build.build()
-    import chunked_gated_delta_08_gb300 as m
-    return m
-
-
 def declared_symbols():
     src = open(os.path.join(ROOT, "include", "gdr.h")).read()
     return sorted(set(re.findall(r"^\s*(?:int|int64_t|const char \*)\s*(gdr_\w+)\s*\(", src, re.M)))

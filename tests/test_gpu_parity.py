@@ -19,14 +19,6 @@ TOL = {torch.float32: 1e-5, torch.bfloat16: 5e-3}
 ALGOS = ["chunked", "auto"]
 
 
-@pytest.fixture(scope="module")
-def gdr():
-    from chunked_gated_delta_08_gb300 import _build
-    _build.build()
-    import chunked_gated_delta_08_gb300 as m
-    return m
-
-
 def rel_l2(got, want):
     got = got.detach().double().cpu().numpy() if hasattr(got, "detach") else np.asarray(got, np.float64)
     want = np.asarray(want, np.float64)
