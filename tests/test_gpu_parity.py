@@ -139,6 +139,11 @@ def test_unit_grid(gdr, case, C, dtype, algo):
     for l2, use_h0 in ((True, True), (False, False)):
         _, x = wl.random_case(B, T, H, HV, K, V, dtype=dtype, lengths=lengths, gate_per_k=per_k,
                               use_h0=use_h0, seed=T + K)
+        if not l2:
+            # the in-kernel norm is off: q, k arrive normalized, as the coverage guide's
+            # use_qk_l2norm_in_kernel=False axis prepares them (section 三)
+            x["q"] = torch.nn.functional.normalize(x["q"].float(), dim=-1).to(dtype)
+            x["k"] = torch.nn.functional.normalize(x["k"].float(), dim=-1).to(dtype)
         o, ht = run_gpu(gdr, x, C, l2, algo)
         ref = run_ref(x, l2)
         assert_parity(o, ht, ref, dtype, f"{case} C={C} l2={l2} h0={use_h0}")

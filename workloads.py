@@ -71,7 +71,14 @@ KDA_BF16_VARLEN = Workload("kda_bf16_varlen_T16384_HV32_V256", torch.bfloat16, B
                            gate_per_k=True, gate_div=4.0, h0_scale=0.1, grads=True)
 
 WORKLOADS = [GDN_FP32_SMALL, GDN_BF16_GVA_K60, GDN_BF16_VARLEN, GDN_BF16_LARGE, KDA_BF16_VARLEN]
-BY_NAME = {w.name: w for w in WORKLOADS}
+
+# A quarter of the large dense workload (B = 1): the same per-unit work on 32
+# blocks, with inputs (3 x 256 MB) still larger than L2.  Used for profiler
+# captures, which replay a kernel many times.
+GDN_BF16_PROFILE = Workload("gdn_bf16_B1_T32768_H32_K128", torch.bfloat16, B=1, T=32768, H=32, HV=32,
+                            K=128, V=128, use_qk_l2norm=True, h0_scale=None)
+
+BY_NAME = {w.name: w for w in WORKLOADS + [GDN_BF16_PROFILE]}
 
 
 def make_inputs(w: Workload, device="cpu", seed: int | None = None) -> dict:
