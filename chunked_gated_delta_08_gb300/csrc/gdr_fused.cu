@@ -23,13 +23,15 @@
 // 128-byte swizzle and are read by the tensor cores K-major and MN-major as
 // they land.
 //
-// Warp roles (320 threads):
-//   warps 0-3  chain: the state recurrence of chunk c (v_new epilogue, state
-//              update, output epilogue) -- the sequential critical path;
-//   warps 4-7  prep: everything of chunk c+1 that does not need the state
-//              (norms, gate cumsum, A, the solve, W', U', w, P);
-//   warp 8     producer: TMA loads of q, k (3-slot ring) and v (1 slot), g, beta;
-//   warp 9     MMA issuer: one thread issues every tcgen05.mma in a fixed order.
+// Warp roles (512 threads):
+//   warps 0-3   chain: the state recurrence of chunk c -- the v_new epilogue,
+//               the decay of the fp32 state held in TMEM (the next MMA adds
+//               dH into it), and the bf16 copy of the new state;
+//   warps 4-11  prep: everything of chunk c that does not need the state
+//               (norms, gate cumsum, A, the solve, W', U', w, P) plus the
+//               output epilogue of chunk c-1;
+//   warp 12     producer: TMA loads of q, k (3-slot ring) and v (1 slot), g, beta;
+//   warp 13     MMA issuer: one thread issues every tcgen05.mma in a fixed order.
 // Hand-offs are mbarriers, each completing once per chunk.  Every wait is
 // bounded by the global timer; on expiry the block records GDR_ERR_TIMEOUT in
 // the status word, lets its copies and MMAs in flight finish, frees its
@@ -59,11 +61,13 @@ constexpr int C = 64;
 constexpr int DK = 128;
 constexpr int DV = 128;
 constexpr int kQKSlots = 3;
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kPrepWarps = 8;
+constexpr int kPrepThreads = 32 * kPrepWarps;
+constexpr int kProducerWarp = 4 + kPrepWarps;
+constexpr int kMmaWarp = kProducerWarp + 1;
+constexpr int kThreads = 512;  // 16 warps: the last two only join the final barrier
 constexpr int kBarChain = 1;   // named barrier of warps 0-3
-constexpr int kBarPrep = 2;    // named barrier of warps 4-7
+constexpr int kBarPrep = 2;    // named barrier of the prep warps
 constexpr int LDA = C + 1;     // row stride of the packed fp32 A / T^T matrix
 
 // shared memory map (offsets from a 1024-byte aligned base)
@@ -80,18 +84,21 @@ constexpr uint32_t OFF_AT = OFF_VT + 16384;          // fp32 [64][65]: A strictl
 constexpr uint32_t OFF_SMALL = (OFF_AT + C * LDA * 4 + 1023) & ~1023u;
 
 // TMEM columns
-constexpr uint32_t TM_S = 0, TM_W = 64, TM_VN = 128, TM_O1 = 192, TM_O2 = 256, TM_H = 320, TM_COLS = 512;
+// TM_HS holds the fp32 state h; the state-update MMA accumulates dH into it.
+constexpr uint32_t TM_S = 0, TM_W = 64, TM_VN = 128, TM_O1 = 192, TM_O2 = 256, TM_HS = 320, TM_COLS = 512;
 
 struct Small {
   float gb[kQKSlots][2][C];     // g, beta of each QK slot (producer)
-  float gam[C], rq[C], rk[C];   // prep: gate cumsum and norm scales
+  float gam[C], rq[C], rk[C];   // prep: gate cumsum and norm scales (0 past the chunk end)
+  float bw[C];                  // prep: beta (0 past the chunk end)
   float ep[C], em[C];           // prep: decay factors e^{G - m}, e^{m - G}
+  float eg[C];                  // prep: e^{G}
   float sv[3][C];               // chain: row scale of vt, rk_i e^{G_L - G_i} (0 past the end)
   float so[3][C];               // chain: row scale of o1, rq_r e^{G_r}
   float gL[4];                  // chain: G at the chunk's last valid row
   float X[3 * 256];             // solve scratch
   uint64_t full_qk[kQKSlots], empty_qk[kQKSlots], full_v, empty_v;
-  uint64_t b_s, b_prep, b_w, b_wepi, b_pend, b_vn, b_vnepi, b_h, b_state, b_oepi, b_final;
+  uint64_t b_s, b_prep, b_w, b_wepi, b_pend, b_vn, b_vnepi, b_h, b_state, b_final;
   uint32_t tmem_slot;
   int err;
   int bad;
@@ -116,8 +123,9 @@ struct FusedParams {
 // T = (I + A)^-1 for a unit lower-triangular 64 x 64 system.  AT holds A
 // strictly below the diagonal; T (strictly lower part; its diagonal is 1) is
 // written transposed strictly above the diagonal: T_ij at AT[j][i].  16 x 16
-// diagonal blocks by forward substitution, then T_bj = -T_bb sum_{l=j}^{b-1}
-// A_bl T_lj level by level.  Threads 0..127 of the prep warpgroup.
+// diagonal blocks by forward substitution (64 threads, one column each), then
+// T_bj = -T_bb sum_{l=j}^{b-1} A_bl T_lj level by level, one output of each
+// block per thread.  Threads 0..255 of the prep warps.
 __device__ __forceinline__ float t_at(const float *AT, int r, int s) {  // T[r][s]
   return r > s ? AT[s * LDA + r] : (r == s ? 1.f : 0.f);
 }
@@ -128,40 +136,50 @@ __device__ void solve_unit_lower(float *AT, float *X, int pt) {
     float x[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      float acc = (i == c) ? 1.f : 0.f;
+      float a0 = (i == c) ? 1.f : 0.f, a1 = 0.f;
 #pragma unroll
-      for (int l = 0; l < i; ++l) acc = fmaf(-AT[(base + i) * LDA + base + l], x[l], acc);
-      x[i] = (i < c) ? 0.f : acc;
+      for (int l = 0; l < i; l += 2) {
+        a0 = fmaf(-AT[(base + i) * LDA + base + l], x[l], a0);
+        if (l + 1 < i) a1 = fmaf(-AT[(base + i) * LDA + base + l + 1], x[l + 1], a1);
+      }
+      x[i] = (i < c) ? 0.f : a0 + a1;
     }
 #pragma unroll
     for (int i = 1; i < 16; ++i)
       if (i > c) AT[(base + c) * LDA + base + i] = x[i];
   }
-  named_bar(kBarPrep, 128);
+  named_bar(kBarPrep, kPrepThreads);
+  const int i = pt >> 4, j = pt & 15;
   for (int d = 1; d <= 3; ++d) {
     const int nb = 4 - d;
-    for (int o = pt; o < nb * 256; o += 128) {
-      const int bi = o >> 8, b = d + bi, j0 = b - d, i = (o >> 4) & 15, j = o & 15;
-      float acc = 0.f;
+    for (int k = 0; k < nb; ++k) {
+      const int b = d + k, j0 = k;
+      float acc0 = 0.f, acc1 = 0.f;
       for (int l = j0; l < b; ++l) {
 #pragma unroll
-        for (int m = 0; m < 16; ++m) acc = fmaf(AT[(16 * b + i) * LDA + 16 * l + m], t_at(AT, 16 * l + m, 16 * j0 + j), acc);
+        for (int m = 0; m < 16; m += 2) {
+          acc0 = fmaf(AT[(16 * b + i) * LDA + 16 * l + m], t_at(AT, 16 * l + m, 16 * j0 + j), acc0);
+          acc1 = fmaf(AT[(16 * b + i) * LDA + 16 * l + m + 1], t_at(AT, 16 * l + m + 1, 16 * j0 + j), acc1);
+        }
       }
-      X[bi * 256 + i * 16 + j] = acc;
+      X[k * 256 + i * 16 + j] = acc0 + acc1;
     }
-    named_bar(kBarPrep, 128);
-    for (int o = pt; o < nb * 256; o += 128) {
-      const int bi = o >> 8, b = d + bi, j0 = b - d, i = (o >> 4) & 15, j = o & 15;
-      float acc = 0.f;
+    named_bar(kBarPrep, kPrepThreads);
+    for (int k = 0; k < nb; ++k) {
+      const int b = d + k, j0 = k;
+      float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-      for (int m = 0; m < 16; ++m) acc = fmaf(t_at(AT, 16 * b + i, 16 * b + m), X[bi * 256 + m * 16 + j], acc);
-      AT[(16 * j0 + j) * LDA + 16 * b + i] = -acc;
+      for (int m = 0; m < 16; m += 2) {
+        acc0 = fmaf(t_at(AT, 16 * b + i, 16 * b + m), X[k * 256 + m * 16 + j], acc0);
+        acc1 = fmaf(t_at(AT, 16 * b + i, 16 * b + m + 1), X[k * 256 + (m + 1) * 16 + j], acc1);
+      }
+      AT[(16 * j0 + j) * LDA + 16 * b + i] = -(acc0 + acc1);
     }
-    named_bar(kBarPrep, 128);
+    named_bar(kBarPrep, kPrepThreads);
   }
 }
 
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
     gdr_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const FusedParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -221,45 +239,49 @@ __global__ void __maxnreg__(200)
 
   if (warp < 4) {
     // ================================================================ chain
-    const int t = tid;  // TMEM lane; state row d = t; output column v = t
+    const int t = tid;  // TMEM lane: state row d = t, v_new column v = t
     const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
     auto vote_wait = [&](uint64_t *bar, uint32_t parity) -> bool {
       return named_bar_and(kBarChain, 128, mbar_wait(smem_u32(bar), parity, err, tmo));
     };
-    float h[DV];
+    // h_0 into TMEM (fp32) and its bf16 copy into sH
     {
       const float *src = p.h0 ? p.h0 + (unit * DK + t) * DV : nullptr;
 #pragma unroll
-      for (int v = 0; v < DV; ++v) h[v] = src ? src[v] : 0.f;
+      for (int q8 = 0; q8 < 8; ++q8) {
+        float r16[16];
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) st_sw128_chunk(sH + (ch >> 3) * 16384, t, ch & 7, pack8(h + 8 * ch));
+        for (int j = 0; j < 16; ++j) r16[j] = src ? src[16 * q8 + j] : 0.f;
+        tmem_st16(lane_addr + TM_HS + 16 * q8, r16);
+        st_sw128_chunk(sH + (q8 >> 2) * 16384, t, (2 * q8) & 7, pack8(r16));
+        st_sw128_chunk(sH + (q8 >> 2) * 16384, t, (2 * q8 + 1) & 7, pack8(r16 + 8));
+      }
+      tmem_st_wait();
     }
     fence_proxy_async_smem();
+    tc_fence_before();
     named_bar(kBarChain, 128);
-    if (t == 0) {  // h_0 is ready; D_vn, D_o1, D_o2 are free
+    if (t == 0) {  // h_0 is ready; D_vn is free
       mbar_arrive(smem_u32(&S.b_state));
-      mbar_arrive(smem_u32(&S.b_oepi));
       mbar_arrive(smem_u32(&S.b_vnepi));
     }
     bool ok = true;
     for (int c = 0; c < nch; ++c) {
       const uint32_t ph = c & 1;
       const int k3 = c % 3;
-      const int64_t t0 = bos + (int64_t)c * C;
-      const int L = (int)(eos - t0 < C ? eos - t0 : C);
       // the prep warps' w-epilogue arrival orders their scalar writes before our reads
       if (!(ok = vote_wait(&S.b_vn, ph) && vote_wait(&S.b_wepi, ph))) break;
       tc_fence_after();
       // ---- vn^T [v][i] and vt^T [v][i] = vn * sv_i
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float r16[16];
-        tmem_ld16(lane_addr + TM_VN + 16 * q4, r16);
+      for (int h2 = 0; h2 < 2; ++h2) {
+        float r32[32];
+        tmem_ld32(lane_addr + TM_VN + 32 * h2, r32);
         tmem_ld_wait();
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int i0 = 16 * q4 + 8 * half;
-          const float *x = r16 + 8 * half;
+        for (int q = 0; q < 4; ++q) {
+          const int i0 = 32 * h2 + 8 * q;
+          const float *x = r32 + 8 * q;
           const float *sc = S.sv[k3] + i0;
           float y[8];
 #pragma unroll
@@ -268,215 +290,248 @@ __global__ void __maxnreg__(200)
           st_sw128_chunk(sVT, t, i0 >> 3, pack8(y));
         }
       }
+      // ---- decay the fp32 state in TMEM; the next MMA adds dH into it
+      {
+        const float decay = __expf(S.gL[k3]);
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {
+          float r16[16];
+          tmem_ld16(lane_addr + TM_HS + 16 * q8, r16);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) r16[j] *= decay;
+          tmem_st16(lane_addr + TM_HS + 16 * q8, r16);
+        }
+        tmem_st_wait();
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       named_bar(kBarChain, 128);
       if (t == 0) mbar_arrive(smem_u32(&S.b_vnepi));
       if (!(ok = vote_wait(&S.b_h, ph))) break;
       tc_fence_after();
-      // ---- state update: h = e^{G_L} h + dH (row d = t), bf16 copy for the next products
-      {
-        const float decay = __expf(S.gL[k3]);
+      // ---- bf16 copy of the new state for the next chunk's products
 #pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) {
-          float r16[16];
-          tmem_ld16(lane_addr + TM_H + 16 * q8, r16);
-          tmem_ld_wait();
+      for (int h4 = 0; h4 < 4; ++h4) {
+        float r32[32];
+        tmem_ld32(lane_addr + TM_HS + 32 * h4, r32);
+        tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) h[16 * q8 + j] = fmaf(decay, h[16 * q8 + j], r16[j]);
-          st_sw128_chunk(sH + (q8 >> 2) * 16384, t, (2 * q8) & 7, pack8(h + 16 * q8));
-          st_sw128_chunk(sH + (q8 >> 2) * 16384, t, (2 * q8 + 1) & 7, pack8(h + 16 * q8 + 8));
+        for (int q = 0; q < 4; ++q) {
+          const int ch = 4 * h4 + q;
+          st_sw128_chunk(sH + (ch >> 3) * 16384, t, ch & 7, pack8(r32 + 8 * q));
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       named_bar(kBarChain, 128);
       if (t == 0) mbar_arrive(smem_u32(&S.b_state));
-      // ---- output: o[r][v] = so_r o1[v][r] + o2[v][r]  (column v = t)
-      {
-        __nv_bfloat16 *ocol = p.o + (t0 * p.HV + hv) * DV + t;
-        const float *so = S.so[k3];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          float a16[16], b16[16];
-          tmem_ld16(lane_addr + TM_O1 + 16 * q4, a16);
-          tmem_ld16(lane_addr + TM_O2 + 16 * q4, b16);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int r = 16 * q4 + j;
-            if (r < L) ocol[(int64_t)r * p.HV * DV] = __float2bfloat16_rn(fmaf(so[r], a16[j], b16[j]));
-          }
-        }
-      }
-      tc_fence_before();
-      named_bar(kBarChain, 128);
-      if (t == 0) mbar_arrive(smem_u32(&S.b_oepi));
     }
     if (named_bar_and(kBarChain, 128, ok && *err == 0) && p.ht) {
       float *dst = p.ht + (unit * DK + t) * DV;
 #pragma unroll
-      for (int v = 0; v < DV; v += 4) *reinterpret_cast<float4 *>(dst + v) = make_float4(h[v], h[v + 1], h[v + 2], h[v + 3]);
+      for (int h4 = 0; h4 < 4; ++h4) {
+        float r32[32];
+        tmem_ld32(lane_addr + TM_HS + 32 * h4, r32);
+        tmem_ld_wait();
+#pragma unroll
+        for (int v = 0; v < 32; v += 4)
+          *reinterpret_cast<float4 *>(dst + 32 * h4 + v) = make_float4(r32[v], r32[v + 1], r32[v + 2], r32[v + 3]);
+      }
     }
-  } else if (warp < 8) {
-    // ================================================================ prep
-    const int pt = tid - 128;  // TMEM lane
-    const uint32_t lane_addr = tbase + ((uint32_t)((warp - 4) * 32) << 16);
+  } else if (warp < 4 + kPrepWarps) {
+    // ================================================================ prep (+ output epilogue)
+    const int pt = tid - 128;                       // 0..255
+    const int quad = warp & 3;                      // TMEM lane quadrant
+    const int lrow = quad * 32 + lane;              // TMEM lane of this thread
+    const int colh = (warp - 4) >> 2;               // which half of the columns this warp reads
+    const uint32_t lane_addr = tbase + ((uint32_t)(quad * 32) << 16);
     float *AT = reinterpret_cast<float *>(sm + OFF_AT);
     auto vote_wait = [&](uint64_t *bar, uint32_t parity) -> bool {
-      return named_bar_and(kBarPrep, 128, mbar_wait(smem_u32(bar), parity, err, tmo));
+      return named_bar_and(kBarPrep, kPrepThreads, mbar_wait(smem_u32(bar), parity, err, tmo));
     };
+    // output epilogue of chunk cc: o[r][v] = so_r o1[v][r] + o2[v][r]; lane v, columns r of this half
+    auto output_epilogue = [&](int cc) {
+      const int64_t t0 = bos + (int64_t)cc * C;
+      const int L = (int)(eos - t0 < C ? eos - t0 : C);
+      const float *so = S.so[cc % 3];
+      float a32[32], b32[32];
+      tmem_ld32(lane_addr + TM_O1 + 32 * colh, a32);
+      tmem_ld32(lane_addr + TM_O2 + 32 * colh, b32);
+      tmem_ld_wait();
+      __nv_bfloat16 *ocol = p.o + (t0 * p.HV + hv) * DV + lrow;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int r = 32 * colh + j;
+        if (r < L) ocol[(int64_t)r * p.HV * DV] = __float2bfloat16_rn(fmaf(so[r], a32[j], b32[j]));
+      }
+    };
+    bool ok = true;
     for (int c = 0; c < nch; ++c) {
       const uint32_t ph = c & 1, php = (c - 1) & 1;
       const int slot = c % kQKSlots, k3 = c % 3;
       const int64_t t0 = bos + (int64_t)c * C;
       const int L = (int)(eos - t0 < C ? eos - t0 : C);
       uint8_t *qk = sm + OFF_QK + slot * SZ_QK;
-      if (!vote_wait(&S.b_s, ph)) break;
+      if (!(ok = vote_wait(&S.b_s, ph))) break;
       tc_fence_after();
       // ragged tail: clear rows past the sequence end (they may hold the next sequence)
       if (L < C) {
-        if (!vote_wait(&S.full_v, ph)) break;
-        for (int e = pt; e < (C - L) * 48; e += 128) {
+        if (!(ok = vote_wait(&S.full_v, ph))) break;
+        for (int e = pt; e < (C - L) * 48; e += kPrepThreads) {
           const int rr = L + e / 48, rest = e % 48, tile = rest >> 3, ch = rest & 7;
           uint8_t *base = tile < 4 ? qk + tile * 8192 : sm + OFF_V + (tile - 4) * 8192;
           st_sw128_chunk(base, rr, ch, make_uint4(0, 0, 0, 0));
         }
         fence_proxy_async_smem();
       }
-      // ---- row norms (q rows on lanes 0-63, k rows on 64-127) and the gate cumsum
+      // ---- q row norms (4 threads per row), k row norms from diag(K K^T), gate cumsum
       {
-        const int row = pt & 63;
-        const uint8_t *base = qk + (pt < 64 ? 8192 : 0);
+        const int row = pt >> 2, part = pt & 3;
+        const uint8_t *qb = qk + 8192 + (part >> 1) * 16384;
         float ss = 0.f;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          ss += sumsq_bf16x8(ld_sw128_chunk(base, row, ch));
-          ss += sumsq_bf16x8(ld_sw128_chunk(base + 16384, row, ch));
-        }
-        const float r = p.l2 ? rsqrtf(ss + kL2Eps) : 1.f;
-        if (pt < 64) S.rq[row] = r;
-        else S.rk[row] = r;
-        if (pt < 64) {
-          float x = S.gb[slot][0][pt];
+        for (int ch = 0; ch < 4; ++ch) ss += sumsq_bf16x8(ld_sw128_chunk(qb, row, 4 * (part & 1) + ch));
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+        if (part == 0) S.rq[row] = row < L ? (p.l2 ? rsqrtf(ss + kL2Eps) : 1.f) : 0.f;
+        if (warp == 4) {
+          float x0 = S.gb[slot][0][lane], x1 = S.gb[slot][0][lane + 32];
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
+            const float y0 = __shfl_up_sync(0xffffffffu, x0, o), y1 = __shfl_up_sync(0xffffffffu, x1, o);
+            if (lane >= o) {
+              x0 += y0;
+              x1 += y1;
+            }
           }
-          S.gam[pt] = x;
+          x1 += __shfl_sync(0xffffffffu, x0, 31);
+          S.gam[lane] = x0;
+          S.gam[lane + 32] = x1;
+        }
+        if (colh == 0 && quad < 2) {  // lanes 0-63 of S hold K K^T; its diagonal is |k_i|^2
+          const int i = lrow;
+          float r32[32];
+          tmem_ld32(lane_addr + TM_S + 32 * (i >> 5), r32);
+          tmem_ld_wait();
+          float kk = 0.f;
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (e == (i & 31)) kk = r32[e];
+          S.rk[i] = i < L ? (p.l2 ? rsqrtf(kk + kL2Eps) : 1.f) : 0.f;
         }
       }
-      named_bar(kBarPrep, 128);
-      if (pt >= 32 && pt < 64) S.gam[pt] += S.gam[31];
-      named_bar(kBarPrep, 128);
+      named_bar(kBarPrep, kPrepThreads);
       {
         const float g0 = S.gam[0], gl = S.gam[L - 1];
         const float m = 0.5f * (g0 + gl);
-        const bool factored = (g0 - gl) <= 160.f;
         if (pt < 64) {
           const float gi = S.gam[pt];
           S.sv[k3][pt] = pt < L ? S.rk[pt] * __expf(gl - gi) : 0.f;
           S.so[k3][pt] = S.rq[pt] * __expf(gi);
           S.ep[pt] = __expf(gi - m);
+          S.eg[pt] = __expf(gi);
           S.em[pt] = __expf(m - gi);
+          S.bw[pt] = pt < L ? S.gb[slot][1][pt] : 0.f;
           if (pt == 0) {
             S.gL[k3] = gl;
-            S.factored = factored;
+            S.factored = (g0 - gl) <= 160.f;
           }
         }
       }
-      named_bar(kBarPrep, 128);
+      named_bar(kBarPrep, kPrepThreads);
       const bool factored = S.factored;
-      // ---- A (rows 0-63 of S): A_ij = beta_i rk_i rk_j e^{G_i - G_j} (k_i . k_j), i > j
-      if (pt < 64) {
-        const int i = pt;
-        const float bi = (i < L ? S.gb[slot][1][i] : 0.f) * S.rk[i];
-        const float epi = S.ep[i], gi = S.gam[i];
+      // ---- A (lanes 0-63 of S): A_ij = beta_i rk_i rk_j e^{G_i - G_j} (k_i . k_j), i > j
+      if (quad < 2) {
+        const int i = lrow;
+        const float bi = S.bw[i] * S.rk[i], epi = S.ep[i], gi = S.gam[i];
+        float r32[32];
+        tmem_ld32(lane_addr + TM_S + 32 * colh, r32);
+        tmem_ld_wait();
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          float r16[16];
-          tmem_ld16(lane_addr + TM_S + 16 * q4, r16);
-          tmem_ld_wait();
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int j = 16 * q4 + jj;
-            if (j < i) {
-              const float dec = factored ? epi * S.em[j] : __expf(gi - S.gam[j]);
-              AT[i * LDA + j] = bi * S.rk[j] * dec * r16[jj];
-            }
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = 32 * colh + jj;
+          if (j < i) {
+            const float dec = factored ? epi * S.em[j] : __expf(gi - S.gam[j]);
+            AT[i * LDA + j] = bi * S.rk[j] * dec * r32[jj];
           }
         }
       }
-      named_bar(kBarPrep, 128);
+      named_bar(kBarPrep, kPrepThreads);
       // ---- T = (I + A)^-1
       solve_unit_lower(AT, S.X, pt);
       // ---- W' = T diag(beta e^G rk), U' = T diag(beta) into the w region once w(c-1) is consumed
-      if (c > 0 && !vote_wait(&S.b_vn, php)) break;
+      if (c > 0 && !(ok = vote_wait(&S.b_vn, php))) break;
       {
-        const int i = pt >> 1, jh = pt & 1;
+        const int i = pt >> 2, jq = pt & 3;  // row i, columns 16 jq .. 16 jq + 15
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           float wv[8], uv[8];
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
-            const int j = 32 * jh + 8 * cc + jj;
-            const float tij = t_at(AT, i, j);
-            const float b = j < L ? S.gb[slot][1][j] : 0.f;
-            uv[jj] = tij * b;
-            wv[jj] = tij * b * __expf(S.gam[j]) * S.rk[j];
+            const int j = 16 * jq + 8 * cc + jj;
+            const float tb = t_at(AT, i, j) * S.bw[j];
+            uv[jj] = tb;
+            wv[jj] = tb * S.eg[j] * S.rk[j];
           }
-          const int ch = 4 * jh + cc;
+          const int ch = 2 * jq + cc;
           st_sw128_chunk(sWU, i, ch, pack8(wv));
           st_sw128_chunk(sWU + 8192, i, ch, pack8(uv));
         }
       }
       fence_proxy_async_smem();
-      named_bar(kBarPrep, 128);
+      named_bar(kBarPrep, kPrepThreads);
       if (pt == 0) mbar_arrive(smem_u32(&S.b_prep));
-      // ---- w [d][i] (MN-major B operand) from w^T in TMEM (lane d)
-      if (!vote_wait(&S.b_w, ph)) break;
+      // ---- w [d][i] (MN-major B operand) from w^T in TMEM (lane d, this half of i)
+      if (!(ok = vote_wait(&S.b_w, ph))) break;
       tc_fence_after();
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float r16[16];
-        tmem_ld16(lane_addr + TM_W + 16 * q4, r16);
+      {
+        float r32[32];
+        tmem_ld32(lane_addr + TM_W + 32 * colh, r32);
         tmem_ld_wait();
-        st_sw128_chunk(sWU, pt, 2 * q4, pack8(r16));
-        st_sw128_chunk(sWU, pt, 2 * q4 + 1, pack8(r16 + 8));
+#pragma unroll
+        for (int q = 0; q < 4; ++q) st_sw128_chunk(sWU, lrow, 4 * colh + q, pack8(r32 + 8 * q));
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      named_bar(kBarPrep, 128);
+      named_bar(kBarPrep, kPrepThreads);
       if (pt == 0) mbar_arrive(smem_u32(&S.b_wepi));
-      // ---- P (rows 64-127 of S) once P(c-1) is consumed
-      if (c > 0 && !vote_wait(&S.b_h, php)) break;
-      if (pt >= 64) {
-        const int r = pt - 64;
-        const float qr = r < L ? S.rq[r] : 0.f, epr = S.ep[r], gr = S.gam[r];
+      // ---- output of chunk c-1 and P of chunk c, once MMA_o2(c-1) has consumed P(c-1)
+      if (c > 0) {
+        if (!(ok = vote_wait(&S.b_h, php))) break;
+        tc_fence_after();
+        output_epilogue(c - 1);
+      }
+      if (quad >= 2) {
+        const int r = lrow - 64;
+        const float qr = S.rq[r], epr = S.ep[r], gr = S.gam[r];
+        float r32[32];
+        tmem_ld32(lane_addr + TM_S + 32 * colh, r32);
+        tmem_ld_wait();
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          float r16[16];
-          tmem_ld16(lane_addr + TM_S + 16 * q4, r16);
-          tmem_ld_wait();
+        for (int q = 0; q < 4; ++q) {
+          float e[8];
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            float e[8];
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-              const int j = 16 * q4 + 8 * half + jj;
-              const float dec = factored ? epr * S.em[j] : __expf(gr - S.gam[j]);
-              e[jj] = j <= r ? qr * S.rk[j] * dec * r16[8 * half + jj] : 0.f;
-            }
-            st_sw128_chunk(sP, r, 2 * q4 + half, pack8(e));
+          for (int jj = 0; jj < 8; ++jj) {
+            const int j = 32 * colh + 8 * q + jj;
+            const float dec = factored ? epr * S.em[j] : __expf(gr - S.gam[j]);
+            e[jj] = j <= r ? qr * S.rk[j] * dec * r32[8 * q + jj] : 0.f;
           }
+          st_sw128_chunk(sP, r, 4 * colh + q, pack8(e));
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      named_bar(kBarPrep, 128);
+      named_bar(kBarPrep, kPrepThreads);
+      // b_pend also tells the issuer that D_o1, D_o2 of chunk c-1 have been read
       if (pt == 0) mbar_arrive(smem_u32(&S.b_pend));
     }
+    // output of the last chunk
+    if (ok && nch > 0 && vote_wait(&S.b_h, (nch - 1) & 1)) {
+      tc_fence_after();
+      output_epilogue(nch - 1);
+    }
+    tc_fence_before();
   } else if (warp == kProducerWarp) {
     // ================================================================ producer
     if (lane == 0) {
@@ -573,7 +628,7 @@ __global__ void __maxnreg__(200)
           issue_s(c + 1);
         }
         // (c) vn^T -= h^T w^T ; o1^T = h^T Q^T
-        if (!(wt(&S.b_wepi, ph) && wt(&S.b_state, ph) && wt(&S.b_oepi, ph))) break;
+        if (!(wt(&S.b_wepi, ph) && wt(&S.b_state, ph) && wt(&S.b_pend, ph))) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
@@ -589,8 +644,8 @@ __global__ void __maxnreg__(200)
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          mma_bf16(tbase + TM_H, smem_desc(aQK + ks * 2048, 16384, 1024), smem_desc(aVT + ks * 32, 16, 1024), id_h,
-                   ks > 0);
+          mma_bf16(tbase + TM_HS, smem_desc(aQK + ks * 2048, 16384, 1024), smem_desc(aVT + ks * 32, 16, 1024),
+                   id_h, 1);
           mma_bf16(tbase + TM_O2, smem_desc(aVN + ks * 32, 16, 1024), smem_desc(aP + ks * 32, 16, 1024), id_kk,
                    ks > 0);
         }

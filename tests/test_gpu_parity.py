@@ -208,11 +208,13 @@ def test_chunk_intermediates(gdr, per_k):
 def test_resume_from_final_state(gdr):
     _, x = wl.random_case(2, 300, 1, 2, 64, 64, dtype=torch.float32, seed=3)
     d = to_dev(x)
-    o, ht = gdr.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0=d["h0"], chunk_size=64)
+    o, ht = gdr.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0=d["h0"], chunk_size=64, use_qk_l2norm=True)
     t1 = 131
     sl = lambda t, a, b: t[:, a:b].contiguous()
-    o1, h1 = gdr.fwd(*[sl(d[k], 0, t1) for k in ("q", "k", "v", "g", "beta")], h0=d["h0"], chunk_size=64)
-    o2, h2 = gdr.fwd(*[sl(d[k], t1, 300) for k in ("q", "k", "v", "g", "beta")], h0=h1, chunk_size=64)
+    o1, h1 = gdr.fwd(*[sl(d[k], 0, t1) for k in ("q", "k", "v", "g", "beta")], h0=d["h0"], chunk_size=64,
+                     use_qk_l2norm=True)
+    o2, h2 = gdr.fwd(*[sl(d[k], t1, 300) for k in ("q", "k", "v", "g", "beta")], h0=h1, chunk_size=64,
+                     use_qk_l2norm=True)
     assert rel_l2(torch.cat([o1, o2], 1), o.double().cpu().numpy()) <= 1e-5
     assert rel_l2(h2, ht.double().cpu().numpy()) <= 1e-5
 
