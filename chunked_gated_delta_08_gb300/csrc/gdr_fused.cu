@@ -96,7 +96,7 @@ struct Small {
   float sv[3][C];               // chain: row scale of vt, rk_i e^{G_L - G_i} (0 past the end)
   float so[3][C];               // chain: row scale of o1, rq_r e^{G_r}
   float gL[4];                  // chain: G at the chunk's last valid row
-  float X[3 * 256];             // solve scratch
+  float X[32 * 32];             // solve scratch
   uint64_t full_qk[kQKSlots], empty_qk[kQKSlots], full_v, empty_v;
   uint64_t b_s, b_prep, b_w, b_wepi, b_pend, b_vn, b_vnepi, b_h, b_state, b_final;
   uint32_t tmem_slot;
@@ -122,17 +122,36 @@ struct FusedParams {
 
 // T = (I + A)^-1 for a unit lower-triangular 64 x 64 system.  AT holds A
 // strictly below the diagonal; T (strictly lower part; its diagonal is 1) is
-// written transposed strictly above the diagonal: T_ij at AT[j][i].  16 x 16
-// diagonal blocks by forward substitution (64 threads, one column each), then
-// T_bj = -T_bb sum_{l=j}^{b-1} A_bl T_lj level by level, one output of each
-// block per thread.  Threads 0..255 of the prep warps.
+// written transposed strictly above the diagonal: T_ij at AT[j][i].  The
+// inverse is built by doubling the block size, with
+// [[T1, 0], [T21, T2]], T21 = -T2 A21 T1 at each step:
+//   16 x 16 diagonal blocks by forward substitution (CUDA cores, fp32);
+//   16 -> 32 and 32 -> 64 by warp-level tensor-core products in split tf32.
+// Threads 0..255 of the prep warps (pw = prep warp 0..7).
 __device__ __forceinline__ float t_at(const float *AT, int r, int s) {  // T[r][s]
   return r > s ? AT[s * LDA + r] : (r == s ? 1.f : 0.f);
 }
 
+// D (16 x 8 tile at A-rows ar0.., B-cols bc0..) = A_tile(rows, k) * B(k, cols)
+// over nk k-steps of 8; A and B read through the functors fa(r, k), fb(k, n).
+template <typename FA, typename FB>
+__device__ __forceinline__ void tile_product(float (&d)[4], int nk, FA fa, FB fb) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) d[e] = 0.f;
+  for (int ks = 0; ks < nk; ++ks) {
+    const int k0 = 8 * ks;
+    const float a[4] = {fa(g, k0 + t), fa(g + 8, k0 + t), fa(g, k0 + t + 4), fa(g + 8, k0 + t + 4)};
+    const float b[2] = {fb(k0 + t, g), fb(k0 + t + 4, g)};
+    mma_3xtf32(d, a, b);
+  }
+}
+
 __device__ void solve_unit_lower(float *AT, float *X, int pt) {
-  if (pt < 64) {
-    const int b = pt >> 4, c = pt & 15, base = 16 * b;
+  const int pw = pt >> 5, lane = pt & 31, g = lane >> 2, t = lane & 3;
+  // ---- 16 x 16 diagonal blocks: prep warp b, lane c < 16 solves column c
+  if (pw < 4 && lane < 16) {
+    const int base = 16 * pw, c = lane;
     float x[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -149,34 +168,56 @@ __device__ void solve_unit_lower(float *AT, float *X, int pt) {
       if (i > c) AT[(base + c) * LDA + base + i] = x[i];
   }
   named_bar(kBarPrep, kPrepThreads);
-  const int i = pt >> 4, j = pt & 15;
-  for (int d = 1; d <= 3; ++d) {
-    const int nb = 4 - d;
-    for (int k = 0; k < nb; ++k) {
-      const int b = d + k, j0 = k;
-      float acc0 = 0.f, acc1 = 0.f;
-      for (int l = j0; l < b; ++l) {
-#pragma unroll
-        for (int m = 0; m < 16; m += 2) {
-          acc0 = fmaf(AT[(16 * b + i) * LDA + 16 * l + m], t_at(AT, 16 * l + m, 16 * j0 + j), acc0);
-          acc1 = fmaf(AT[(16 * b + i) * LDA + 16 * l + m + 1], t_at(AT, 16 * l + m + 1, 16 * j0 + j), acc1);
-        }
-      }
-      X[k * 256 + i * 16 + j] = acc0 + acc1;
-    }
-    named_bar(kBarPrep, kPrepThreads);
-    for (int k = 0; k < nb; ++k) {
-      const int b = d + k, j0 = k;
-      float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-      for (int m = 0; m < 16; m += 2) {
-        acc0 = fmaf(t_at(AT, 16 * b + i, 16 * b + m), X[k * 256 + m * 16 + j], acc0);
-        acc1 = fmaf(t_at(AT, 16 * b + i, 16 * b + m + 1), X[k * 256 + (m + 1) * 16 + j], acc1);
-      }
-      AT[(16 * j0 + j) * LDA + 16 * b + i] = -(acc0 + acc1);
-    }
-    named_bar(kBarPrep, kPrepThreads);
+  // ---- 16 -> 32: T_{b,b-1} = -T_bb (A_{b,b-1} T_{b-1,b-1}) for b = 1, 3 (warps 0-3: pair, n-tile)
+  if (pw < 4) {
+    const int b = 1 + 2 * (pw >> 1), nt = pw & 1, r0 = 16 * b, c0 = 16 * (b - 1);
+    float *Z = X + (pw >> 1) * 256;  // Z [16][16]
+    float d[4];
+    tile_product(d, 2, [&](int r, int k) { return AT[(r0 + r) * LDA + c0 + k]; },
+                 [&](int k, int n) { return t_at(AT, c0 + k, c0 + 8 * nt + n); });
+    Z[g * 16 + 8 * nt + 2 * t] = d[0];
+    Z[g * 16 + 8 * nt + 2 * t + 1] = d[1];
+    Z[(g + 8) * 16 + 8 * nt + 2 * t] = d[2];
+    Z[(g + 8) * 16 + 8 * nt + 2 * t + 1] = d[3];
   }
+  named_bar(kBarPrep, kPrepThreads);
+  if (pw < 4) {
+    const int b = 1 + 2 * (pw >> 1), nt = pw & 1, r0 = 16 * b, c0 = 16 * (b - 1);
+    const float *Z = X + (pw >> 1) * 256;
+    float d[4];
+    tile_product(d, 2, [&](int r, int k) { return t_at(AT, r0 + r, r0 + k); },
+                 [&](int k, int n) { return Z[k * 16 + 8 * nt + n]; });
+    const int cc = c0 + 8 * nt + 2 * t;
+    AT[cc * LDA + r0 + g] = -d[0];
+    AT[(cc + 1) * LDA + r0 + g] = -d[1];
+    AT[cc * LDA + r0 + g + 8] = -d[2];
+    AT[(cc + 1) * LDA + r0 + g + 8] = -d[3];
+  }
+  named_bar(kBarPrep, kPrepThreads);
+  // ---- 32 -> 64: Y = A[32:64, 0:32] T[0:32, 0:32]; T[32:64, 0:32] = -T[32:64, 32:64] Y (8 warps, one 16 x 8 tile each)
+  {
+    const int mt = pw >> 2, nt = pw & 3;
+    float d[4];
+    tile_product(d, 4, [&](int r, int k) { return AT[(32 + 16 * mt + r) * LDA + k]; },
+                 [&](int k, int n) { return t_at(AT, k, 8 * nt + n); });
+    X[(16 * mt + g) * 32 + 8 * nt + 2 * t] = d[0];
+    X[(16 * mt + g) * 32 + 8 * nt + 2 * t + 1] = d[1];
+    X[(16 * mt + g + 8) * 32 + 8 * nt + 2 * t] = d[2];
+    X[(16 * mt + g + 8) * 32 + 8 * nt + 2 * t + 1] = d[3];
+  }
+  named_bar(kBarPrep, kPrepThreads);
+  {
+    const int mt = pw >> 2, nt = pw & 3;
+    float d[4];
+    tile_product(d, 4, [&](int r, int k) { return t_at(AT, 32 + 16 * mt + r, 32 + k); },
+                 [&](int k, int n) { return X[k * 32 + 8 * nt + n]; });
+    const int cc = 8 * nt + 2 * t, rr = 32 + 16 * mt + g;
+    AT[cc * LDA + rr] = -d[0];
+    AT[(cc + 1) * LDA + rr] = -d[1];
+    AT[cc * LDA + rr + 8] = -d[2];
+    AT[(cc + 1) * LDA + rr + 8] = -d[3];
+  }
+  named_bar(kBarPrep, kPrepThreads);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
