@@ -37,7 +37,7 @@ GDR_F32, GDR_BF16 = 0, 1
 GDR_GATE_SCALAR, GDR_GATE_PER_K = 0, 1
 ALGOS = {"auto": 0, "chunked": 1, "fused": 2}
 
-EXPORTED = ["gdr_fwd", "gdr_chunked_sizes_get", "gdr_chunk_index", "gdr_chunk_prepare", "gdr_chunk_fwd_h",
+EXPORTED = ["gdr_fwd", "gdr_fwd_noalloc", "gdr_chunked_sizes_get", "gdr_chunk_index", "gdr_chunk_prepare", "gdr_chunk_fwd_h",
             "gdr_chunk_fwd_o", "gdr_device_status", "gdr_last_error", "gdr_launch_count", "gdr_version"]
 
 
@@ -68,6 +68,7 @@ def _load():
     P, I = ctypes.c_void_p, ctypes.c_int
     D = ctypes.POINTER(GdrDesc)
     lib.gdr_fwd.argtypes = [D, P, P, P, P, P, P, P, I, I, P, P, P]
+    lib.gdr_fwd_noalloc.argtypes = [D, P, P, P, P, P, P, P, I, I, P, P, P]
     lib.gdr_chunked_sizes_get.argtypes = [D, I, I, ctypes.POINTER(GdrChunkedSizes)]
     lib.gdr_chunk_index.argtypes = [D, P, I, P, P, P]
     lib.gdr_chunk_prepare.argtypes = [D, P, P, P, P, P, P, I, I, P, P, P, P]

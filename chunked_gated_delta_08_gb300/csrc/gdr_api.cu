@@ -156,6 +156,12 @@ int run_chunked(const gdr_desc &d, const void *q, const void *k, const void *v, 
 
 }  // namespace
 
+int validate_request(const gdr_desc *d, int chunk_size, const int64_t *cu) { return validate(d, chunk_size, cu); }
+
+void chunked_scratch_sizes(const gdr_desc &d, int C, const int64_t *cu, gdr_chunked_sizes *s) {
+  sizes_of(d, C, cu, s);
+}
+
 int *device_status_word(int dev, int *err) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g_status[dev]) {

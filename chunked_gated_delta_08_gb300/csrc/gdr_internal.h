@@ -45,6 +45,11 @@ struct ChunkedArgs {
   cudaStream_t stream;
 };
 
+// Argument checks shared by the entry points, and the chunked form's scratch
+// sizes (gdr_api.cu).
+int validate_request(const gdr_desc *d, int chunk_size, const int64_t *cu);
+void chunked_scratch_sizes(const gdr_desc &d, int C, const int64_t *cu, gdr_chunked_sizes *s);
+
 // Launchers of the chunked (three-kernel) form; return GDR_OK or an error.
 int launch_chunk_index(const ChunkedArgs &a);
 int launch_chunk_prepare(const ChunkedArgs &a);

@@ -140,6 +140,33 @@ int gdr_chunk_fwd_o(const gdr_desc *desc, const void *q, const void *k, const fl
                     void *stream);
 
 /*
+ * gdr_fwd_noalloc -- the chunked forward without any device allocation.
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory: code whose framework allocator owns all
+ * device memory, code running where allocation calls are forbidden or would
+ * synchronize, and callers that must not allocate after start-up.  It takes
+ * the same arguments as gdr_fwd and computes the same results as gdr_fwd with
+ * GDR_ALGO_CHUNKED (desc->algo is ignored).  Its scratch is one fixed device
+ * array of GDR_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds
+ * until the process exits; requests needing more return GDR_ERR_SHAPE with a
+ * message giving both sizes (about 2.6 KB per token and value head at
+ * K = V = 128, so e.g. 1024 tokens x 16 heads fit).
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array: calls whose work overlaps on the GPU
+ *     (concurrent streams, or several host threads) race and corrupt each
+ *     other's results; serialize them.  Every scratch byte a call reads it
+ *     first writes, so nothing carries over from one call to the next.
+ *   - No status word exists for this path: with invalid cu_seqlens the
+ *     outputs are left untouched and nothing is recorded.
+ */
+#define GDR_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int gdr_fwd_noalloc(const gdr_desc *desc, const void *q, const void *k, const void *v, const float *g,
+                    const void *beta, const float *h0, const int64_t *cu_seqlens, int chunk_size,
+                    int use_qk_l2norm, void *o, float *ht, void *stream);
+
+/*
  * gdr_device_status -- synchronizes `stream`, then returns (and, if `clear`,
  * resets) the library's device-side status word for the current device:
  * GDR_OK, GDR_ERR_SEQLENS or GDR_ERR_TIMEOUT.  Also returns GDR_ERR_CUDA if
