@@ -33,7 +33,7 @@
 //   warp 12     producer: TMA loads of q, k (3-slot ring) and v (1 slot), g, beta;
 //   warp 13     MMA issuer: one thread issues every tcgen05.mma in a fixed order.
 // Hand-offs are mbarriers, each completing once per chunk.  Every wait is
-// bounded by the global timer; on expiry the block records GDR_ERR_TIMEOUT in
+// bounded (about two seconds of SM clock); on expiry the block records GDR_ERR_TIMEOUT in
 // the status word, lets its copies and MMAs in flight finish, frees its
 // tensor memory and returns.  A role's decision to stop is uniform across
 // its threads.
@@ -92,7 +92,7 @@ struct Small {
   float gam[C], rq[C], rk[C];   // prep: gate cumsum and norm scales (0 past the chunk end)
   float bw[C];                  // prep: beta (0 past the chunk end)
   float ep[C], em[C];           // prep: decay factors e^{G - m}, e^{m - G}
-  float eg[C];                  // prep: e^{G}
+  float cw[C];                  // prep: column scale of W', beta_j e^{G_j} rk_j
   float sv[3][C];               // chain: row scale of vt, rk_i e^{G_L - G_i} (0 past the end)
   float so[3][C];               // chain: row scale of o1, rq_r e^{G_r}
   float gL[4];                  // chain: G at the chunk's last valid row
@@ -117,7 +117,7 @@ struct FusedParams {
   int *status;
   int64_t T, N, H, HV;
   int l2;
-  unsigned long long timeout_ns;
+  unsigned long long timeout_cycles;
 };
 
 // T = (I + A)^-1 for a unit lower-triangular 64 x 64 system.  AT holds A
@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = S.tmem_slot;
   volatile int *err = &S.err;
-  const uint64_t tmo = p.timeout_ns;
+  const uint64_t tmo = p.timeout_cycles;
   uint8_t *const sH = sm + OFF_H, *const sWU = sm + OFF_WU, *const sP = sm + OFF_P, *const sVN = sm + OFF_VN,
                  *const sVT = sm + OFF_VT;
 
@@ -282,8 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ chain
     const int t = tid;  // TMEM lane: state row d = t, v_new column v = t
     const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
+    // one thread polls; the others sleep in the named barrier that shares its verdict
     auto vote_wait = [&](uint64_t *bar, uint32_t parity) -> bool {
-      return named_bar_and(kBarChain, 128, mbar_wait(smem_u32(bar), parity, err, tmo));
+      const bool ok = t == 0 ? mbar_wait(smem_u32(bar), parity, err, tmo) : true;
+      return named_bar_and(kBarChain, 128, ok);
     };
     // h_0 into TMEM (fp32) and its bf16 copy into sH
     {
@@ -316,17 +318,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- vn^T [v][i] and vt^T [v][i] = vn * sv_i
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
-        float r32[32];
+        // every load of this block before any store: the stores could alias them otherwise
+        float r32[32], sc[32];
         tmem_ld32(lane_addr + TM_VN + 32 * h2, r32);
+        ld_f32x32(S.sv[k3] + 32 * h2, sc);
         tmem_ld_wait();
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int i0 = 32 * h2 + 8 * q;
           const float *x = r32 + 8 * q;
-          const float *sc = S.sv[k3] + i0;
           float y[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) y[e] = x[e] * sc[e];
+          for (int e = 0; e < 8; ++e) y[e] = x[e] * sc[8 * q + e];
           st_sw128_chunk(sVN, t, i0 >> 3, pack8(x));
           st_sw128_chunk(sVT, t, i0 >> 3, pack8(y));
         }
@@ -389,23 +392,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = tbase + ((uint32_t)(quad * 32) << 16);
     float *AT = reinterpret_cast<float *>(sm + OFF_AT);
     auto vote_wait = [&](uint64_t *bar, uint32_t parity) -> bool {
-      return named_bar_and(kBarPrep, kPrepThreads, mbar_wait(smem_u32(bar), parity, err, tmo));
+      const bool ok = pt == 0 ? mbar_wait(smem_u32(bar), parity, err, tmo) : true;
+      return named_bar_and(kBarPrep, kPrepThreads, ok);
     };
     // output epilogue of chunk cc: o[r][v] = so_r o1[v][r] + o2[v][r]; lane v, columns r of this half
     auto output_epilogue = [&](int cc) {
       const int64_t t0 = bos + (int64_t)cc * C;
       const int L = (int)(eos - t0 < C ? eos - t0 : C);
-      const float *so = S.so[cc % 3];
-      float a32[32], b32[32];
+      float a32[32], b32[32], so[32];
       tmem_ld32(lane_addr + TM_O1 + 32 * colh, a32);
       tmem_ld32(lane_addr + TM_O2 + 32 * colh, b32);
+      ld_f32x32(S.so[cc % 3] + 32 * colh, so);
       tmem_ld_wait();
-      __nv_bfloat16 *ocol = p.o + (t0 * p.HV + hv) * DV + lrow;
+      __nv_bfloat16 ov[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int r = 32 * colh + j;
-        if (r < L) ocol[(int64_t)r * p.HV * DV] = __float2bfloat16_rn(fmaf(so[r], a32[j], b32[j]));
-      }
+      for (int j = 0; j < 32; ++j) ov[j] = __float2bfloat16_rn(fmaf(so[j], a32[j], b32[j]));
+      const int64_t rstride = p.HV * DV;
+      __nv_bfloat16 *ocol = p.o + (t0 * p.HV + hv) * DV + lrow + (int64_t)(32 * colh) * rstride;
+      const int nr = L - 32 * colh;  // rows of this half that exist
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < nr) ocol[(int64_t)j * rstride] = ov[j];
     };
     bool ok = true;
     for (int c = 0; c < nch; ++c) {
@@ -471,9 +478,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           S.sv[k3][pt] = pt < L ? S.rk[pt] * __expf(gl - gi) : 0.f;
           S.so[k3][pt] = S.rq[pt] * __expf(gi);
           S.ep[pt] = __expf(gi - m);
-          S.eg[pt] = __expf(gi);
           S.em[pt] = __expf(m - gi);
-          S.bw[pt] = pt < L ? S.gb[slot][1][pt] : 0.f;
+          const float bw = pt < L ? S.gb[slot][1][pt] : 0.f;
+          S.bw[pt] = bw;
+          S.cw[pt] = bw * __expf(gi) * S.rk[pt];
           if (pt == 0) {
             S.gL[k3] = gl;
             S.factored = (g0 - gl) <= 160.f;
@@ -486,16 +494,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (quad < 2) {
         const int i = lrow;
         const float bi = S.bw[i] * S.rk[i], epi = S.ep[i], gi = S.gam[i];
-        float r32[32];
-        tmem_ld32(lane_addr + TM_S + 32 * colh, r32);
-        tmem_ld_wait();
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int j = 32 * colh + jj;
-          if (j < i) {
-            const float dec = factored ? epi * S.em[j] : __expf(gi - S.gam[j]);
-            AT[i * LDA + j] = bi * S.rk[j] * dec * r32[jj];
+        for (int h16 = 0; h16 < 2; ++h16) {
+          const int j0 = 32 * colh + 16 * h16;
+          float r16[16], f[16], rk[16];
+          tmem_ld16(lane_addr + TM_S + j0, r16);
+          ld_f32x16(S.rk + j0, rk);
+          if (factored) {
+            ld_f32x16(S.em + j0, f);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) f[jj] *= epi;
+          } else {
+            ld_f32x16(S.gam + j0, f);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) f[jj] = __expf(gi - f[jj]);
           }
+          tmem_ld_wait();
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj)
+            if (j0 + jj < i) AT[i * LDA + j0 + jj] = bi * rk[jj] * f[jj] * r16[jj];
         }
       }
       named_bar(kBarPrep, kPrepThreads);
@@ -504,21 +521,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- W' = T diag(beta e^G rk), U' = T diag(beta) into the w region once w(c-1) is consumed
       if (c > 0 && !(ok = vote_wait(&S.b_vn, php))) break;
       {
-        const int i = pt >> 2, jq = pt & 3;  // row i, columns 16 jq .. 16 jq + 15
+        const int i = pt >> 2, j0 = 16 * (pt & 3);  // row i, columns j0 .. j0 + 15
+        float tv[16], bw[16], cw[16];
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          float wv[8], uv[8];
+        for (int jj = 0; jj < 16; ++jj) tv[jj] = t_at(AT, i, j0 + jj);
+        ld_f32x16(S.bw + j0, bw);
+        ld_f32x16(S.cw + j0, cw);
+        float wv[16], uv[16];
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const int j = 16 * jq + 8 * cc + jj;
-            const float tb = t_at(AT, i, j) * S.bw[j];
-            uv[jj] = tb;
-            wv[jj] = tb * S.eg[j] * S.rk[j];
-          }
-          const int ch = 2 * jq + cc;
-          st_sw128_chunk(sWU, i, ch, pack8(wv));
-          st_sw128_chunk(sWU + 8192, i, ch, pack8(uv));
+        for (int jj = 0; jj < 16; ++jj) {
+          uv[jj] = tv[jj] * bw[jj];
+          wv[jj] = tv[jj] * cw[jj];
         }
+        st_sw128_chunk(sWU, i, j0 >> 3, pack8(wv));
+        st_sw128_chunk(sWU, i, (j0 >> 3) + 1, pack8(wv + 8));
+        st_sw128_chunk(sWU + 8192, i, j0 >> 3, pack8(uv));
+        st_sw128_chunk(sWU + 8192, i, (j0 >> 3) + 1, pack8(uv + 8));
       }
       fence_proxy_async_smem();
       named_bar(kBarPrep, kPrepThreads);
@@ -546,19 +564,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (quad >= 2) {
         const int r = lrow - 64;
         const float qr = S.rq[r], epr = S.ep[r], gr = S.gam[r];
-        float r32[32];
-        tmem_ld32(lane_addr + TM_S + 32 * colh, r32);
-        tmem_ld_wait();
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float e[8];
+        for (int h16 = 0; h16 < 2; ++h16) {
+          const int j0 = 32 * colh + 16 * h16;
+          float r16[16], f[16], rk[16];
+          tmem_ld16(lane_addr + TM_S + j0, r16);
+          ld_f32x16(S.rk + j0, rk);
+          if (factored) {
+            ld_f32x16(S.em + j0, f);
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const int j = 32 * colh + 8 * q + jj;
-            const float dec = factored ? epr * S.em[j] : __expf(gr - S.gam[j]);
-            e[jj] = j <= r ? qr * S.rk[j] * dec * r32[8 * q + jj] : 0.f;
+            for (int jj = 0; jj < 16; ++jj) f[jj] *= epr;
+          } else {
+            ld_f32x16(S.gam + j0, f);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) f[jj] = __expf(gr - f[jj]);
           }
-          st_sw128_chunk(sP, r, 4 * colh + q, pack8(e));
+          tmem_ld_wait();
+          float e[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) e[jj] = j0 + jj <= r ? qr * rk[jj] * f[jj] * r16[jj] : 0.f;
+          st_sw128_chunk(sP, r, j0 >> 3, pack8(e));
+          st_sw128_chunk(sP, r, (j0 >> 3) + 1, pack8(e + 8));
         }
       }
       fence_proxy_async_smem();
@@ -584,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < nch; ++c) {
       const int slot = c % kQKSlots, u = c / kQKSlots;
       if (c >= kQKSlots) {
-        const bool ok = mbar_wait(smem_u32(&S.empty_qk[slot]), (u - 1) & 1, err, tmo);
+        const bool ok = lane == 0 ? mbar_wait(smem_u32(&S.empty_qk[slot]), (u - 1) & 1, err, tmo) : true;
         if (!__all_sync(0xffffffffu, ok)) break;
       }
       const int64_t t0 = bos + (int64_t)c * C;
@@ -607,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(smem_u32(&S.full_qk[slot]));
       issued_qk = c + 1;
       if (c >= 1) {
-        const bool ok = mbar_wait(smem_u32(&S.empty_v), (c - 1) & 1, err, tmo);
+        const bool ok = lane == 0 ? mbar_wait(smem_u32(&S.empty_v), (c - 1) & 1, err, tmo) : true;
         if (!__all_sync(0xffffffffu, ok)) break;
       }
       if (lane == 0) {
@@ -776,7 +802,7 @@ int run_fused(const gdr_desc &d, const void *q, const void *k, const void *v, co
   fp.H = d.H;
   fp.HV = d.HV;
   fp.l2 = l2;
-  fp.timeout_ns = 2000000000ull;
+  fp.timeout_cycles = 1ull << 32;  // about two seconds at GB300 clocks
   cudaError_t e = cudaFuncSetAttribute(gdr_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(gdr_fused_kernel)");
   gdr_fused_kernel<<<(unsigned)(d.N * d.HV), kThreads, SMEM_BYTES, stream>>>(mq, mk, mv, fp);

@@ -31,6 +31,28 @@ __device__ __forceinline__ uint4 ld_sw128_chunk(const uint8_t *tile, uint32_t ro
   return *reinterpret_cast<const uint4 *>(tile + sw128_chunk_off(row, chunk));
 }
 
+// Batched vector loads of 16 / 32 consecutive floats (16-byte aligned).
+__device__ __forceinline__ void ld_f32x16(const float *src, float (&d)[16]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 v = reinterpret_cast<const float4 *>(src)[q];
+    d[4 * q] = v.x;
+    d[4 * q + 1] = v.y;
+    d[4 * q + 2] = v.z;
+    d[4 * q + 3] = v.w;
+  }
+}
+__device__ __forceinline__ void ld_f32x32(const float *src, float (&d)[32]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float4 v = reinterpret_cast<const float4 *>(src)[q];
+    d[4 * q] = v.x;
+    d[4 * q + 1] = v.y;
+    d[4 * q + 2] = v.z;
+    d[4 * q + 3] = v.w;
+  }
+}
+
 __device__ __forceinline__ float sumsq_bf16x8(uint4 u) {
   const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&u);
   float s = 0.f;

@@ -52,6 +52,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// The same with a suspend-time hint: the thread may sleep in the instruction
+// until the phase completes or about `ns` nanoseconds pass, instead of
+// spinning and taking issue slots from the warps doing the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
@@ -59,18 +73,19 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Waits for the phase with the given parity to complete, for at most
-// `timeout_ns` nanoseconds.  Returns false if the time ran out (after setting
+// Waits for the phase with the given parity to complete.  The bound is in SM
+// clock cycles (clock64 is cheap to read; 2^32 cycles is about two seconds at
+// the GB300's clocks).  Returns false if the bound ran out (after setting
 // *err) or if another thread has already set *err; the caller must then stop
 // waiting on anything and wind down.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *err, uint64_t timeout_ns) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *err, uint64_t max_cycles) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  const uint64_t t0 = clock64();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if ((i & 15u) == 0) {
       if (*err) return false;
-      if (globaltimer_ns() - t0 > timeout_ns) {
+      if ((uint64_t)clock64() - t0 > max_cycles) {
         *err = 1;
         return false;
       }
@@ -80,11 +95,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 
 // The same wait, ignoring the shared error flag (used while winding down to
 // let copies already in flight land before the block exits).
-__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
-  const uint64_t t0 = globaltimer_ns();
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t max_cycles) {
+  const uint64_t t0 = clock64();
   for (uint32_t i = 0;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 63u && globaltimer_ns() - t0 > timeout_ns) return false;
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if ((i & 15u) == 15u && (uint64_t)clock64() - t0 > max_cycles) return false;
   }
 }
 
