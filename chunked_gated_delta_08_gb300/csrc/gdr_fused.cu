@@ -98,7 +98,7 @@ struct Small {
   float gL[4];                  // chain: G at the chunk's last valid row
   float X[32 * 32];             // solve scratch
   uint64_t full_qk[kQKSlots], empty_qk[kQKSlots], full_v, empty_v;
-  uint64_t b_s, b_prep, b_w, b_wepi, b_pend, b_vn, b_vnepi, b_h, b_state, b_final;
+  uint64_t b_s, b_sfree, b_prep, b_w, b_wepi, b_pend, b_vn, b_vnepi, b_h, b_state, b_final;
   uint32_t tmem_slot;
   int err;
   int bad;
@@ -222,7 +222,8 @@ __device__ void solve_unit_lower(float *AT, float *X, int pt) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     gdr_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const FusedParams p) {
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                     const FusedParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Small &S = *reinterpret_cast<Small *>(sm + OFF_SMALL);
@@ -391,11 +392,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int colh = (warp - 4) >> 2;               // which half of the columns this warp reads
     const uint32_t lane_addr = tbase + ((uint32_t)(quad * 32) << 16);
     float *AT = reinterpret_cast<float *>(sm + OFF_AT);
+    uint8_t *const sO = sm + OFF_AT;  // bf16 output staging [r][v] (2 swizzled sub-tiles) once A / T are done
     auto vote_wait = [&](uint64_t *bar, uint32_t parity) -> bool {
       const bool ok = pt == 0 ? mbar_wait(smem_u32(bar), parity, err, tmo) : true;
       return named_bar_and(kBarPrep, kPrepThreads, ok);
     };
-    // output epilogue of chunk cc: o[r][v] = so_r o1[v][r] + o2[v][r]; lane v, columns r of this half
+    // output of chunk cc: o[r][v] = so_r o1[v][r] + o2[v][r]; lane v, rows r of this half.  Whole
+    // chunks go through the staging tile and two TMA tensor stores; a ragged last chunk is
+    // stored element by element so nothing past the sequence end is written.
     auto output_epilogue = [&](int cc) {
       const int64_t t0 = bos + (int64_t)cc * C;
       const int L = (int)(eos - t0 < C ? eos - t0 : C);
@@ -407,12 +411,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       __nv_bfloat16 ov[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) ov[j] = __float2bfloat16_rn(fmaf(so[j], a32[j], b32[j]));
-      const int64_t rstride = p.HV * DV;
-      __nv_bfloat16 *ocol = p.o + (t0 * p.HV + hv) * DV + lrow + (int64_t)(32 * colh) * rstride;
-      const int nr = L - 32 * colh;  // rows of this half that exist
+      if (L == C) {
+        uint8_t *tile = sO + (lrow >> 6) * 8192;
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < nr) ocol[(int64_t)j * rstride] = ov[j];
+        for (int j = 0; j < 32; ++j)
+          *reinterpret_cast<__nv_bfloat16 *>(tile + sw128_offset(32 * colh + j, lrow & 63)) = ov[j];
+        fence_proxy_async_smem();
+        named_bar(kBarPrep, kPrepThreads);
+        if (pt == 0) {
+          tma_store_3d(&tm_o, smem_u32(sO), 0, (int)hv, (int)t0);
+          tma_store_3d(&tm_o, smem_u32(sO + 8192), 64, (int)hv, (int)t0);
+          bulk_commit();
+        }
+      } else {
+        const int64_t rstride = p.HV * DV;
+        __nv_bfloat16 *ocol = p.o + (t0 * p.HV + hv) * DV + lrow + (int64_t)(32 * colh) * rstride;
+        const int nr = L - 32 * colh;  // rows of this half that exist
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < nr) ocol[(int64_t)j * rstride] = ov[j];
+      }
     };
     bool ok = true;
     for (int c = 0; c < nch; ++c) {
@@ -487,13 +505,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             S.factored = (g0 - gl) <= 160.f;
           }
         }
+        // the previous chunk's output staging (in the A / T array) must have been read by its TMA store
+        if (pt == 0) bulk_wait_read0();
       }
       named_bar(kBarPrep, kPrepThreads);
       const bool factored = S.factored;
-      // ---- A (lanes 0-63 of S): A_ij = beta_i rk_i rk_j e^{G_i - G_j} (k_i . k_j), i > j
-      if (quad < 2) {
-        const int i = lrow;
-        const float bi = S.bw[i] * S.rk[i], epi = S.ep[i], gi = S.gam[i];
+      // ---- A from lanes 0-63 of S: A_ij = beta_i rk_i rk_j e^{G_i - G_j} (k_i . k_j), i > j;
+      //      P from lanes 64-127: P_rj = rq_r rk_j e^{G_r - G_j} (q_r . k_j), j <= r, kept packed in
+      //      registers until its buffer is free, so S can be overwritten by the next chunk's product.
+      uint32_t pk[16];
+      {
+        const int i = quad < 2 ? lrow : lrow - 64;
+        const float bi = quad < 2 ? S.bw[i] * S.rk[i] : S.rq[i], epi = S.ep[i], gi = S.gam[i];
 #pragma unroll
         for (int h16 = 0; h16 < 2; ++h16) {
           const int j0 = 32 * colh + 16 * h16;
@@ -510,12 +533,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int jj = 0; jj < 16; ++jj) f[jj] = __expf(gi - f[jj]);
           }
           tmem_ld_wait();
+          if (quad < 2) {
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj)
-            if (j0 + jj < i) AT[i * LDA + j0 + jj] = bi * rk[jj] * f[jj] * r16[jj];
+            for (int jj = 0; jj < 16; ++jj)
+              if (j0 + jj < i) AT[i * LDA + j0 + jj] = bi * rk[jj] * f[jj] * r16[jj];
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 16; jj += 2) {
+              const float e0 = j0 + jj <= i ? bi * rk[jj] * f[jj] * r16[jj] : 0.f;
+              const float e1 = j0 + jj + 1 <= i ? bi * rk[jj + 1] * f[jj + 1] * r16[jj + 1] : 0.f;
+              pk[8 * h16 + jj / 2] = pack_bf16(e0, e1);
+            }
+          }
         }
       }
+      tc_fence_before();
       named_bar(kBarPrep, kPrepThreads);
+      if (pt == 0) mbar_arrive(smem_u32(&S.b_sfree));  // S may now take the next chunk's product
       // ---- T = (I + A)^-1
       solve_unit_lower(AT, S.X, pt);
       // ---- W' = T diag(beta e^G rk), U' = T diag(beta) into the w region once w(c-1) is consumed
@@ -541,6 +575,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       named_bar(kBarPrep, kPrepThreads);
       if (pt == 0) mbar_arrive(smem_u32(&S.b_prep));
+      // ---- output of chunk c-1 and P of chunk c, once MMA_o2(c-1) has consumed P(c-1)
+      if (c > 0) {
+        if (!(ok = vote_wait(&S.b_h, php))) break;
+        tc_fence_after();
+        output_epilogue(c - 1);
+      }
+      if (quad >= 2) {
+        const int r = lrow - 64;
+        st_sw128_chunk(sP, r, 4 * colh, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+        st_sw128_chunk(sP, r, 4 * colh + 1, make_uint4(pk[4], pk[5], pk[6], pk[7]));
+        st_sw128_chunk(sP, r, 4 * colh + 2, make_uint4(pk[8], pk[9], pk[10], pk[11]));
+        st_sw128_chunk(sP, r, 4 * colh + 3, make_uint4(pk[12], pk[13], pk[14], pk[15]));
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar(kBarPrep, kPrepThreads);
+      // b_pend: P(c) is in place and D_o1, D_o2 of chunk c-1 have been read
+      if (pt == 0) mbar_arrive(smem_u32(&S.b_pend));
       // ---- w [d][i] (MN-major B operand) from w^T in TMEM (lane d, this half of i)
       if (!(ok = vote_wait(&S.b_w, ph))) break;
       tc_fence_after();
@@ -555,49 +607,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       named_bar(kBarPrep, kPrepThreads);
       if (pt == 0) mbar_arrive(smem_u32(&S.b_wepi));
-      // ---- output of chunk c-1 and P of chunk c, once MMA_o2(c-1) has consumed P(c-1)
-      if (c > 0) {
-        if (!(ok = vote_wait(&S.b_h, php))) break;
-        tc_fence_after();
-        output_epilogue(c - 1);
-      }
-      if (quad >= 2) {
-        const int r = lrow - 64;
-        const float qr = S.rq[r], epr = S.ep[r], gr = S.gam[r];
-#pragma unroll
-        for (int h16 = 0; h16 < 2; ++h16) {
-          const int j0 = 32 * colh + 16 * h16;
-          float r16[16], f[16], rk[16];
-          tmem_ld16(lane_addr + TM_S + j0, r16);
-          ld_f32x16(S.rk + j0, rk);
-          if (factored) {
-            ld_f32x16(S.em + j0, f);
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) f[jj] *= epr;
-          } else {
-            ld_f32x16(S.gam + j0, f);
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) f[jj] = __expf(gr - f[jj]);
-          }
-          tmem_ld_wait();
-          float e[16];
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) e[jj] = j0 + jj <= r ? qr * rk[jj] * f[jj] * r16[jj] : 0.f;
-          st_sw128_chunk(sP, r, j0 >> 3, pack8(e));
-          st_sw128_chunk(sP, r, (j0 >> 3) + 1, pack8(e + 8));
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      named_bar(kBarPrep, kPrepThreads);
-      // b_pend also tells the issuer that D_o1, D_o2 of chunk c-1 have been read
-      if (pt == 0) mbar_arrive(smem_u32(&S.b_pend));
     }
     // output of the last chunk
     if (ok && nch > 0 && vote_wait(&S.b_h, (nch - 1) & 1)) {
       tc_fence_after();
       output_epilogue(nch - 1);
     }
+    if (pt == 0) bulk_wait0();  // every output store has landed before the block can exit
     tc_fence_before();
   } else if (warp == kProducerWarp) {
     // ================================================================ producer
@@ -605,6 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_o);
     }
     int issued_qk = 0, issued_v = 0;
     for (int c = 0; c < nch; ++c) {
@@ -676,7 +693,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ph = c & 1;
         const int slot = c % kQKSlots;
         const uint32_t aQK = smem_u32(sm + OFF_QK + slot * SZ_QK);
-        // (a) w^T = K^T W'^T ; vn^T = V^T U'^T
+        // S of the next chunk as soon as the prep warps have read this one's
+        if (c + 1 < nch) {
+          if (!(wt(&S.b_sfree, ph) && wt(&S.full_qk[(c + 1) % kQKSlots], ((c + 1) / kQKSlots) & 1))) break;
+          tc_fence_after();
+          issue_s(c + 1);
+        }
+        // w^T = K^T W'^T ; vn^T = V^T U'^T
         if (!(wt(&S.b_prep, ph) && wt(&S.full_v, ph) && wt(&S.b_vnepi, ph))) break;
         tc_fence_after();
 #pragma unroll
@@ -688,13 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(smem_u32(&S.b_w));
         mma_commit(smem_u32(&S.empty_v));
-        // (b) S of the next chunk, once the prep warps are done with this one's
-        if (c + 1 < nch) {
-          if (!(wt(&S.b_pend, ph) && wt(&S.full_qk[(c + 1) % kQKSlots], ((c + 1) / kQKSlots) & 1))) break;
-          tc_fence_after();
-          issue_s(c + 1);
-        }
-        // (c) vn^T -= h^T w^T ; o1^T = h^T Q^T
+        // vn^T -= h^T w^T ; o1^T = h^T Q^T
         if (!(wt(&S.b_wepi, ph) && wt(&S.b_state, ph) && wt(&S.b_pend, ph))) break;
         tc_fence_after();
 #pragma unroll
@@ -706,8 +723,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                    ks > 0);
         }
         mma_commit(smem_u32(&S.b_vn));
-        // (d) dH = K^T vt ; o2^T = vn^T P^T
-        if (!(wt(&S.b_vnepi, ph ^ 1) && wt(&S.b_pend, ph))) break;
+        // dH = K^T vt ; o2^T = vn^T P^T
+        if (!wt(&S.b_vnepi, ph ^ 1)) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
@@ -771,8 +788,8 @@ int run_fused(const gdr_desc &d, const void *q, const void *k, const void *v, co
   const int64_t tok = d.B * d.T;
   if (tok >= (int64_t)INT32_MAX) return GDR_ERR_UNSUPPORTED;  // TMA coordinates are int32
   if (d.N * d.HV > (int64_t)INT32_MAX) return GDR_ERR_UNSUPPORTED;
-  if (tok > 0 && !(aligned16(q) && aligned16(k) && aligned16(v)))
-    return set_error(GDR_ERR_ALIGN, "q, k and v must be 16-byte aligned for the fused form");
+  if (tok > 0 && !(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(o)))
+    return set_error(GDR_ERR_ALIGN, "q, k, v and o must be 16-byte aligned for the fused form");
   if (d.N == 0) return GDR_OK;
   if (tok == 0) {
     // no tokens: the final state is the initial one
@@ -784,11 +801,12 @@ int run_fused(const gdr_desc &d, const void *q, const void *k, const void *v, co
     }
     return GDR_OK;
   }
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   int rc;
   if ((rc = fused_make_map(&mq, q, DK, d.H, tok)) != GDR_OK) return rc;
   if ((rc = fused_make_map(&mk, k, DK, d.H, tok)) != GDR_OK) return rc;
   if ((rc = fused_make_map(&mv, v, DV, d.HV, tok)) != GDR_OK) return rc;
+  if ((rc = fused_make_map(&mo, o, DV, d.HV, tok)) != GDR_OK) return rc;
   FusedParams fp;
   fp.beta = (const __nv_bfloat16 *)beta;
   fp.g = g;
@@ -805,7 +823,7 @@ int run_fused(const gdr_desc &d, const void *q, const void *k, const void *v, co
   fp.timeout_cycles = 1ull << 32;  // about two seconds at GB300 clocks
   cudaError_t e = cudaFuncSetAttribute(gdr_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(gdr_fused_kernel)");
-  gdr_fused_kernel<<<(unsigned)(d.N * d.HV), kThreads, SMEM_BYTES, stream>>>(mq, mk, mv, fp);
+  gdr_fused_kernel<<<(unsigned)(d.N * d.HV), kThreads, SMEM_BYTES, stream>>>(mq, mk, mv, mo, fp);
   count_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "gdr_fused_kernel launch");
