@@ -49,6 +49,23 @@ def peaks():
     return {**FALLBACK, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def recorded_traffic(w: wl.Workload, kernel: str):
+    """DRAM bytes per launch from the committed ncu record, if it still describes
+    the kernel as built (same source hash) and this workload; else None."""
+    path = os.path.join(ROOT, "profiles", "gdr_fused_kernel_traffic.json")
+    if kernel != "gdr_fused" or w.name != wl.GDN_BF16_LARGE.name or not os.path.exists(path):
+        return None
+    import hashlib
+    rec = json.load(open(path))
+    h = hashlib.sha256()
+    for f in ("gdr_fused.cu", "gdr_fused_common.cuh", "gdr_sm100.cuh"):
+        with open(os.path.join(ROOT, "chunked_gated_delta_08_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest() != rec.get("kernel_source_sha256"):
+        return None
+    return rec.get("traffic_bytes_per_launch_bench_workload")
+
+
 # ------------------------------------------------------------------ algorithmic work
 def algorithmic_bytes(w: wl.Workload) -> int:
     """Inputs read once, outputs written once (per step, whole workload)."""
@@ -312,7 +329,7 @@ def run_ours(args, w, world, rank, local):
         kms, kbytes = avg_ms[kname], kb[kname]
     achieved = kbytes / (kms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"], "traffic": None, "peak_source": pk["source"],
+                "frac": achieved / pk["hbm_gbs"], "traffic": recorded_traffic(w, kname), "peak_source": pk["source"],
                 "algorithmic_bytes_per_launch": kbytes, "avg_launch_ms": kms}
     spec_us = max(byt / (NOMINAL_HBM_GBS * 1e9), flops / (pk["bf16_tflops"] * 1e12)) * 1e6
     roofline_spec = {"definition": "max(bytes / 8 TB/s, FLOPs / dense bf16 peak) for the whole step",
