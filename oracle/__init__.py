@@ -10,6 +10,8 @@ Contents
                           (sequence, value head)); see ``gdr_oracle.c``.
 * ``gdr_fwd_ref_units``-- the same on a sampled subset of (sequence, head) units,
                           for workloads too large to run whole.
+* ``gdr_bwd_ref``      -- the reverse recurrence: gradients of o and ht with
+                          respect to q, k, v, g, beta and h0 (C, fp64).
 * ``chunk_index_ref``  -- the varlen chunk map (sequence, chunk-in-sequence).
 * ``chunk_form_ref``   -- the chunk-form intermediates A, T = (I + A)^-1, w, u of
                           one chunk, written from their definitions with a numpy
@@ -58,6 +60,10 @@ def load_oracle_lib(path: str):
     lib.gdr_oracle_fwd.argtypes = [i64, i64, i64, i64, i64, i64, ctypes.c_int,
                                    p, p, p, p, p, p, p, i64, ctypes.c_int,
                                    p, p, i64, p, p, ctypes.c_int]
+    lib.gdr_oracle_bwd.restype = ctypes.c_int
+    lib.gdr_oracle_bwd.argtypes = [i64, i64, i64, i64, i64, i64, ctypes.c_int,
+                                   p, p, p, p, p, p, p, i64, ctypes.c_int,
+                                   p, p, p, p, p, p, p, p, ctypes.c_int]
     return lib
 
 
@@ -146,6 +152,38 @@ def gdr_fwd_ref(q, k, v, g, beta, h0=None, cu_seqlens=None, use_qk_l2norm=False,
         out["h_chunks"] = h_chunks
     if v_new is not None:
         out["v_new"] = v_new
+    return out
+
+
+def gdr_bwd_ref(q, k, v, g, beta, do, dht=None, h0=None, cu_seqlens=None, use_qk_l2norm=False,
+                threads=0, lib=None):
+    """Reverse recurrence of the per-token forward, fp64.
+
+    For the loss L = sum(o * do) + sum(ht * dht), returns a dict of numpy fp64
+    arrays ``dq``, ``dk`` [B,T,H,K], ``dv`` [B,T,HV,V], ``dg`` shaped like g,
+    ``dbeta`` [B,T,HV] and ``dh0`` [N,HV,K,V].  Shapes and layouts of the
+    inputs are those of ``gdr_fwd_ref``; ``dht`` None means zero.
+    """
+    lib = lib or _load()
+    q, k, v, g, beta, h0, do, dht = (_f64(x) for x in (q, k, v, g, beta, h0, do, dht))
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    gate_per_k = 1 if g.ndim == 4 else 0
+    cu = None
+    if cu_seqlens is not None:
+        cu = np.ascontiguousarray(np.asarray(
+            cu_seqlens.cpu() if hasattr(cu_seqlens, "cpu") else cu_seqlens, dtype=np.int64))
+        N = len(cu) - 1
+    else:
+        N = B
+    out = {"dq": np.zeros_like(q), "dk": np.zeros_like(k), "dv": np.zeros_like(v), "dg": np.zeros_like(g),
+           "dbeta": np.zeros_like(beta), "dh0": np.zeros((N, HV, K, V))}
+    rc = lib.gdr_oracle_bwd(B, T, H, HV, K, V, gate_per_k, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                            _ptr(h0), _ptr(cu), N, int(bool(use_qk_l2norm)), _ptr(do), _ptr(dht),
+                            _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]),
+                            _ptr(out["dbeta"]), _ptr(out["dh0"]), int(threads))
+    if rc != 0:
+        raise RuntimeError(f"oracle failed with status {rc}")
     return out
 
 

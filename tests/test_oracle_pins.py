@@ -6,6 +6,7 @@ import numpy as np
 import pytest
 
 import oracle
+from tests import oracle_bwd_checks as ob
 from tests import oracle_checks as oc
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -14,6 +15,11 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 @pytest.mark.parametrize("check", oc.ALL_CHECKS, ids=lambda f: f.__name__)
 def test_oracle_pin(check):
     check(oracle.gdr_fwd_ref, np.random.default_rng(1234))
+
+
+@pytest.mark.parametrize("check", ob.ALL_BWD_CHECKS, ids=lambda f: f.__name__)
+def test_oracle_bwd_pin(check):
+    check(oracle.gdr_bwd_ref, oracle.gdr_fwd_ref, np.random.default_rng(4321))
 
 
 def test_chunk_form_per_key_gate():
@@ -63,4 +69,13 @@ def test_golden_regression():
     stored = json.load(open(os.path.join(GOLDEN, "oracle_tiny.json")))
     now = compute()
     for key in ("o", "ht"):
+        np.testing.assert_allclose(np.array(now[key]), np.array(stored[key]), rtol=1e-12, atol=1e-13)
+
+
+def test_golden_bwd_regression():
+    """The reverse recurrence still produces the values its committed generator stored."""
+    from tests.golden.make_golden import compute_bwd
+    stored = json.load(open(os.path.join(GOLDEN, "oracle_bwd_tiny.json")))
+    now = compute_bwd()
+    for key in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
         np.testing.assert_allclose(np.array(now[key]), np.array(stored[key]), rtol=1e-12, atol=1e-13)

@@ -112,9 +112,9 @@ def make_inputs(w: Workload, device="cpu", seed: int | None = None) -> dict:
 
 
 def random_case(B, T, H, HV, K, V, dtype=torch.float32, lengths=None, gate_per_k=False,
-                use_h0=True, seed=0, gate_div=1.0):
+                use_h0=True, seed=0, gate_div=1.0, grads=False):
     """A small unit-test case of arbitrary shape with the same distributions."""
     w = Workload(f"case_{B}_{T}_{H}_{HV}_{K}_{V}", dtype, B, T, H, HV, K, V,
                  lengths=tuple(lengths) if lengths else None, gate_per_k=gate_per_k,
-                 gate_div=gate_div, h0_scale=0.1 if use_h0 else None, seed=seed)
+                 gate_div=gate_div, h0_scale=0.1 if use_h0 else None, seed=seed, grads=grads)
     return w, make_inputs(w)
