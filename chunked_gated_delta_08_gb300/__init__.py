@@ -1,4 +1,4 @@
-"""Python binding of libgdr.so, the GB300 chunked gated delta rule forward.
+"""Python binding of libgdr.so, the GB300 chunked gated delta rule (forward and backward).
 
 Argument marshalling only: every step of the computation runs in the CUDA
 kernels behind the C ABI (``include/gdr.h``).  PyTorch supplies device memory
@@ -7,6 +7,7 @@ this module raises.
 
     o, ht = fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, chunk_size=64,
                 use_qk_l2norm=False, output_final_state=True)
+    dq, dk, dv, dg, dbeta, dh0 = bwd(q, k, v, g, beta, do, dht=None, h0=None, ...)
 
 Layouts: q, k [B,T,H,K]; v [B,T,HV,V]; g [B,T,HV] (GDN) or [B,T,HV,K] (KDA),
 fp32; beta [B,T,HV]; h0 [N,HV,K,V] fp32; cu_seqlens [N+1] int64 (B == 1).
@@ -37,7 +38,7 @@ GDR_F32, GDR_BF16 = 0, 1
 GDR_GATE_SCALAR, GDR_GATE_PER_K = 0, 1
 ALGOS = {"auto": 0, "chunked": 1, "fused": 2}
 
-EXPORTED = ["gdr_fwd", "gdr_fwd_noalloc", "gdr_chunked_sizes_get", "gdr_chunk_index", "gdr_chunk_prepare", "gdr_chunk_fwd_h",
+EXPORTED = ["gdr_fwd", "gdr_bwd", "gdr_fwd_noalloc", "gdr_chunked_sizes_get", "gdr_chunk_index", "gdr_chunk_prepare", "gdr_chunk_fwd_h",
             "gdr_chunk_fwd_o", "gdr_device_status", "gdr_last_error", "gdr_launch_count", "gdr_version"]
 
 
@@ -69,6 +70,7 @@ def _load():
     D = ctypes.POINTER(GdrDesc)
     lib.gdr_fwd.argtypes = [D, P, P, P, P, P, P, P, I, I, P, P, P]
     lib.gdr_fwd_noalloc.argtypes = [D, P, P, P, P, P, P, P, I, I, P, P, P]
+    lib.gdr_bwd.argtypes = [D, P, P, P, P, P, P, P, I, I, P, P, P, P, P, P, P, P, P]
     lib.gdr_chunked_sizes_get.argtypes = [D, I, I, ctypes.POINTER(GdrChunkedSizes)]
     lib.gdr_chunk_index.argtypes = [D, P, I, P, P, P]
     lib.gdr_chunk_prepare.argtypes = [D, P, P, P, P, P, P, I, I, P, P, P, P]
@@ -179,6 +181,36 @@ def fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, chunk_size=64, use_qk_l2norm
                       _stream_ptr(stream))
     _check(rc)
     return o, ht
+
+
+def bwd(q, k, v, g, beta, do, dht=None, h0=None, cu_seqlens=None, chunk_size=64, use_qk_l2norm=False,
+        out=None, stream=None):
+    """Backward of ``fwd`` for L = sum(o * do) + sum(ht * dht).
+
+    Returns ``(dq, dk, dv, dg, dbeta, dh0)``: dq, dk, dv, dbeta in the input
+    dtype, dg (shaped like g) and dh0 ([N,HV,K,V]) in fp32.  ``dht`` None means
+    zero.  ``out`` may give the six output tensors.  The forward's
+    intermediates are recomputed inside the call.
+    """
+    B, T, H, K, HV, V, N = _check_inputs(q, k, v, g, beta, h0, cu_seqlens)
+    _require(do, "do", q.dtype, (B, T, HV, V))
+    _require(dht, "dht", torch.float32, (N, HV, K, V))
+    desc = make_desc(q, v, g, cu_seqlens, "chunked")
+    if out is None:
+        dq, dk = torch.empty_like(q), torch.empty_like(k)
+        dv, dbeta = torch.empty_like(v), torch.empty_like(beta)
+        dg = torch.empty_like(g)
+        dh0 = torch.empty(N, HV, K, V, dtype=torch.float32, device=q.device)
+    else:
+        dq, dk, dv, dg, dbeta, dh0 = out
+        for t, ref, name in ((dq, q, "dq"), (dk, k, "dk"), (dv, v, "dv"), (dg, g, "dg"), (dbeta, beta, "dbeta")):
+            _require(t, name, ref.dtype, ref.shape)
+        _require(dh0, "dh0", torch.float32, (N, HV, K, V))
+    rc = _lib.gdr_bwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                      _ptr(cu_seqlens), int(chunk_size), int(bool(use_qk_l2norm)), _ptr(do), _ptr(dht), _ptr(dq),
+                      _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dh0), _stream_ptr(stream))
+    _check(rc)
+    return dq, dk, dv, dg, dbeta, dh0
 
 
 def fwd_host(q, k, v, g, beta, h0=None, cu_seqlens=None, chunk_size=64, use_qk_l2norm=False,

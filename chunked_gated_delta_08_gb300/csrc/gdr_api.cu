@@ -154,6 +154,74 @@ int run_chunked(const gdr_desc &d, const void *q, const void *k, const void *v, 
   return rc;
 }
 
+// The backward: the forward recompute (chunk index, prepare, fwd_h) into
+// pool scratch, then the five backward kernels.
+int run_bwd(const gdr_desc &d, const void *q, const void *k, const void *v, const float *g, const void *beta,
+            const float *h0, const int64_t *cu, int C, int l2, const void *d_o, const float *dht, void *dq,
+            void *dk, void *dv, float *dg, void *dbeta, float *dh0, cudaStream_t stream) {
+  int dev, rc;
+  if ((rc = current_device(&dev)) != GDR_OK) return rc;
+  int *status = device_status_word(dev, &rc);
+  if (!status) return rc;
+  cudaMemPool_t pool;
+  if ((rc = scratch_pool(dev, &pool)) != GDR_OK) return rc;
+  gdr_chunked_sizes s;
+  sizes_of(d, C, cu, &s);
+  // forward: chunk maps, gcum, w, u, v_new, h; backward: dvn, dhc, dqa, dka, dga, dW
+  const size_t sz[13] = {s.chunk_indices_bytes, s.chunk_offsets_bytes, s.gcum_bytes, s.w_bytes, s.u_bytes,
+                         s.v_new_bytes, s.h_bytes, s.u_bytes, s.h_bytes, s.w_bytes, s.w_bytes, s.gcum_bytes,
+                         s.w_bytes};
+  size_t total = 0;
+  for (size_t x : sz) total += align256(x);
+  char *base = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync((void **)&base, total > 0 ? total : 256, pool, stream);
+  if (e != cudaSuccess) return cuda_error(e, "cudaMallocFromPoolAsync (backward scratch)");
+  char *ptr[13];
+  char *p = base;
+  for (int i = 0; i < 13; ++i) {
+    ptr[i] = p;
+    p += align256(sz[i]);
+  }
+  BwdArgs b{};
+  ChunkedArgs &a = b.f;
+  a.d = d;
+  a.C = C;
+  a.l2 = l2;
+  a.q = q; a.k = k; a.v = v; a.beta = beta; a.g = g; a.h0 = h0; a.cu = cu;
+  a.chunk_indices = cu ? (int64_t *)ptr[0] : nullptr;
+  a.chunk_offsets = cu ? (int64_t *)ptr[1] : nullptr;
+  a.gcum = (float *)ptr[2];
+  a.w = (float *)ptr[3];
+  a.u = (float *)ptr[4];
+  a.v_new = (float *)ptr[5];
+  a.h = (float *)ptr[6];
+  a.ht = nullptr;
+  a.o = nullptr;
+  a.nt_max = s.nt_max;
+  a.status = status;
+  a.stream = stream;
+  b.d_o = d_o;
+  b.dht = dht;
+  b.dvn = (float *)ptr[7];
+  b.dhc = (float *)ptr[8];
+  b.dqa = (float *)ptr[9];
+  b.dka = (float *)ptr[10];
+  b.dga = (float *)ptr[11];
+  b.dW = (float *)ptr[12];
+  b.dq = dq; b.dk = dk; b.dv = dv; b.dbeta = dbeta; b.dg = dg; b.dh0 = dh0;
+  if (cu) rc = launch_chunk_index(a);
+  if (rc == GDR_OK) rc = launch_chunk_prepare(a);
+  if (rc == GDR_OK) rc = launch_chunk_fwd_h(a);
+  if (rc == GDR_OK) rc = launch_bwd_dv_local(b);
+  if (rc == GDR_OK) rc = launch_bwd_dh(b);
+  if (rc == GDR_OK) rc = launch_bwd_dqkg(b);
+  if (rc == GDR_OK) rc = launch_bwd_wy(b);
+  if (rc == GDR_OK) rc = launch_bwd_finalize(b);
+  e = cudaFreeAsync(base, stream);
+  if (rc == GDR_OK && e != cudaSuccess) rc = cuda_error(e, "cudaFreeAsync (backward scratch)");
+  return rc;
+}
+
 }  // namespace
 
 int validate_request(const gdr_desc *d, int chunk_size, const int64_t *cu) { return validate(d, chunk_size, cu); }
@@ -213,6 +281,20 @@ int gdr_fwd(const gdr_desc *desc, const void *q, const void *k, const void *v, c
     }
   }
   return run_chunked(d, q, k, v, g, beta, h0, cu_seqlens, chunk_size, l2, o, ht, s);
+}
+
+int gdr_bwd(const gdr_desc *desc, const void *q, const void *k, const void *v, const float *g, const void *beta,
+            const float *h0, const int64_t *cu_seqlens, int chunk_size, int use_qk_l2norm, const void *d_o,
+            const float *dht, void *dq, void *dk, void *dv, float *dg, void *dbeta, float *dh0, void *stream) {
+  int rc = validate(desc, chunk_size, cu_seqlens);
+  if (rc != GDR_OK) return rc;
+  const gdr_desc &d = *desc;
+  if (d.K > 128) return set_error(GDR_ERR_SHAPE, "gdr_bwd supports K <= 128");
+  const int64_t tok = d.B * d.T;
+  if (tok > 0 && (!q || !k || !v || !g || !beta || !d_o || !dq || !dk || !dv || !dg || !dbeta))
+    return set_error(GDR_ERR_NULLPTR, "q, k, v, g, beta, d_o, dq, dk, dv, dg and dbeta must be non-NULL");
+  return run_bwd(d, q, k, v, g, beta, h0, cu_seqlens, chunk_size, use_qk_l2norm ? 1 : 0, d_o, dht, dq, dk, dv, dg,
+                 dbeta, dh0, (cudaStream_t)stream);
 }
 
 int gdr_chunked_sizes_get(const gdr_desc *desc, int chunk_size, int varlen, gdr_chunked_sizes *out) {

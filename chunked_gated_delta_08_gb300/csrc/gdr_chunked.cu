@@ -100,42 +100,6 @@ __global__ void chunk_index_kernel(const int64_t *__restrict__ cu, int64_t N, in
     }
 }
 
-// Maps a chunk row to (sequence, chunk-in-sequence); false if the row is unused.
-__device__ __forceinline__ bool chunk_coords(const int64_t *chunk_indices, int64_t chunk, int64_t T, int C,
-                                             int64_t *n, int64_t *j) {
-  if (chunk_indices) {
-    *n = chunk_indices[2 * chunk];
-    *j = chunk_indices[2 * chunk + 1];
-    return *n >= 0;
-  }
-  const int64_t ncs = (T + C - 1) / C;
-  *n = chunk / ncs;
-  *j = chunk % ncs;
-  return true;
-}
-
-// Loads one token row of q or k (head hq) into smem, L2-normalized if asked.
-// Called by a whole warp; rows past the chunk's end are zero.
-template <typename Tin>
-__device__ __forceinline__ void load_row_normed(const Tin *__restrict__ x, int64_t tok, int64_t H, int64_t hq,
-                                                int64_t K, bool valid, bool l2, float *dst, int lane) {
-  float r[8];
-  float ss = 0.f;
-#pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    const int64_t d = lane + 32 * m;
-    r[m] = (valid && d < K) ? to_f32(x[(tok * H + hq) * K + d]) : 0.f;
-    ss += r[m] * r[m];
-  }
-  float scale = 1.f;
-  if (l2) scale = rsqrtf(warp_sum(ss) + kL2Eps);
-#pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    const int64_t d = lane + 32 * m;
-    if (d < K) dst[d] = r[m] * scale;
-  }
-}
-
 // --------------------------------------------------------------------------
 // prepare: grid (nt_max, HV)
 // smem: ks[C*K] | gam[C*K or C] | bet[C] | A[C*C]

@@ -45,6 +45,27 @@ struct ChunkedArgs {
   cudaStream_t stream;
 };
 
+// The backward: the forward recompute (prepare, fwd_h) runs through `f`;
+// the rest are the backward's own scratch and outputs.
+struct BwdArgs {
+  ChunkedArgs f;
+  const void *d_o;           // upstream gradient of o [B,T,HV,V], input dtype
+  const float *dht;          // upstream gradient of ht [N,HV,K,V], nullable
+  float *dvn;                // [B*T,HV,V]: dL/dv_new (local part, then complete)
+  float *dhc;                // [NT,HV,K,V]: dL/d(state leaving chunk c)
+  float *dqa, *dka;          // [B*T,HV,K]: dL/dq^, dL/dk^ per value head
+  float *dga;                // [B*T,HV,gw]: dL/dGamma from the output and state terms
+  float *dW;                 // [B*T,HV,K]: dL/dw
+  void *dq, *dk, *dv, *dbeta;  // outputs in the input dtype
+  float *dg, *dh0;           // outputs, fp32 (dh0 nullable)
+};
+
+int launch_bwd_dv_local(const BwdArgs &a);
+int launch_bwd_dh(const BwdArgs &a);
+int launch_bwd_dqkg(const BwdArgs &a);
+int launch_bwd_wy(const BwdArgs &a);
+int launch_bwd_finalize(const BwdArgs &a);
+
 // Argument checks shared by the entry points, and the chunked form's scratch
 // sizes (gdr_api.cu).
 int validate_request(const gdr_desc *d, int chunk_size, const int64_t *cu);

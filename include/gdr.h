@@ -96,6 +96,33 @@ int gdr_fwd(const gdr_desc *desc, const void *q, const void *k, const void *v, c
             int use_qk_l2norm, void *o, float *ht, void *stream);
 
 /*
+ * gdr_bwd -- the backward of gdr_fwd: gradients of L = sum(o * do) +
+ * sum(ht * dht) with respect to q, k, v, g, beta and h0 (the optional
+ * backward of the problem statement; the coverage guide, section 三, grades
+ * dq, dk, dv, dg, dbeta and dh0, and the KCP handbook's debug-script layout
+ * names its chunk stages bwd_dAu -> bwd_dhu -> bwd_dv -> bwd_o -> bwd_wy ->
+ * bwd_dqk_intra).  The forward's intermediates are recomputed, not taken from
+ * a previous call.
+ *   Inputs as gdr_fwd (desc->algo is ignored), plus
+ *   d_o    upstream gradient of o, [B,T,HV,V] in the input dtype;
+ *   dht    upstream gradient of ht, [N,HV,K,V] fp32; NULL means zero.
+ *   Outputs (caller-owned device memory, every element written):
+ *   dq, dk [B,T,H,K], dv [B,T,HV,V], dbeta [B,T,HV] in the input dtype;
+ *   dg shaped like g, fp32; dh0 [N,HV,K,V] fp32, NULL means not wanted
+ *   (it is the gradient with respect to the initial state, zero or not).
+ * With grouped value heads, dq and dk sum over the HV/H value heads that
+ * share a q/k head.  K must be <= 128 (GDR_ERR_SHAPE otherwise).  Scratch
+ * (about 4 K + 5 V floats per token and value head, plus two fp32 states per
+ * chunk and value head) comes from the same library-owned pool as gdr_fwd's.
+ * Invalid cu_seqlens leave the outputs untouched and set GDR_ERR_SEQLENS in
+ * the status word.
+ */
+int gdr_bwd(const gdr_desc *desc, const void *q, const void *k, const void *v, const float *g,
+            const void *beta, const float *h0, const int64_t *cu_seqlens, int chunk_size,
+            int use_qk_l2norm, const void *d_o, const float *dht, void *dq, void *dk, void *dv,
+            float *dg, void *dbeta, float *dh0, void *stream);
+
+/*
  * Stage entry points of the chunked form, with caller-provided scratch, so the
  * per-chunk intermediates can be inspected.  Sizes come from gdr_chunked_sizes.
  *

@@ -111,6 +111,15 @@ def make_inputs(w: Workload, device="cpu", seed: int | None = None) -> dict:
     return out
 
 
+def make_grads(w: Workload, seed: int = 1, device="cpu") -> dict:
+    """Upstream gradients do [B,T,HV,V] (input dtype) and dht [N,HV,K,V] (fp32),
+    N(0,1), for a workload whose own recipe has none."""
+    gen = torch.Generator().manual_seed(seed)
+    do = torch.randn(w.B, w.T, w.HV, w.V, generator=gen).to(w.dtype)
+    dht = torch.randn(w.N, w.HV, w.K, w.V, generator=gen)
+    return {"do": do.to(device), "dht": dht.to(device)}
+
+
 def random_case(B, T, H, HV, K, V, dtype=torch.float32, lengths=None, gate_per_k=False,
                 use_h0=True, seed=0, gate_div=1.0, grads=False):
     """A small unit-test case of arbitrary shape with the same distributions."""
