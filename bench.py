@@ -12,7 +12,11 @@ all heads).  ``value`` times the forward with inputs resident in HBM (inputs
 are 4.3 GB, far larger than the 129 MB L2, so no flush is needed); ``e2e``
 times the public host-buffer call (pinned host -> device copies, the forward,
 device -> host copies of o and ht) every step.  ``--impl reference`` times the
-fp64 CPU oracle on a bounded sample of the same workload.
+fp64 CPU oracle on a bounded sample of the same workload.  On one GPU the line
+also carries ``bwd``: the backward timed on the KDA varlen workload (lengths
+700/324/3072/12288, HV 32, K 128, V 256), against the FP32 CUDA-core peak;
+and ``decode``: one decode step of the per-token form (256 sequences x 1
+token, 32 heads, K = V = 128, state in place) against HBM bandwidth.
 """
 from __future__ import annotations
 
@@ -83,6 +87,18 @@ def algorithmic_flops(w: wl.Workload) -> int:
     """3CK + 2CV + 6KV per token per value head (causal triangles counted as half)."""
     C = w.chunk_size
     return w.B * w.T * w.HV * (3 * C * w.K + 2 * C * w.V + 6 * w.K * w.V)
+
+
+def bwd_algorithmic_flops(w: wl.Workload) -> int:
+    """10CK + 5CV + 16KV per token per value head: the chunk-form backward's
+    products (forward recompute included, causal triangles counted as half)."""
+    C = w.chunk_size
+    return w.B * w.T * w.HV * (10 * C * w.K + 5 * C * w.V + 16 * w.K * w.V)
+
+
+def fp32_alu_tflops(sm_mhz: float) -> float:
+    """FP32 FMA peak: 152 SMs x 128 lanes x 2 FLOP x the SM clock."""
+    return 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
 
 
 # ------------------------------------------------------------------ clocks
@@ -278,6 +294,88 @@ def stage_timings(gdr, w, d, steps):
     return avg_ms, kbytes
 
 
+def bwd_measurement(gdr, steps: int, warmup: int = 3):
+    """The backward on the KDA varlen workload (its graded configuration),
+    inputs resident, CUDA events on the launching stream."""
+    w = wl.KDA_BF16_VARLEN
+    x = {k: (None if t is None else t.cuda()) for k, t in wl.make_inputs(w).items()}
+    s = torch.cuda.current_stream()
+    outs = (torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"]),
+            torch.empty_like(x["g"]), torch.empty_like(x["beta"]),
+            torch.empty(w.N, w.HV, w.K, w.V, dtype=torch.float32, device="cuda"))
+
+    def call():
+        gdr.bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["do"], dht=x["dht"], h0=x["h0"],
+                cu_seqlens=x["cu_seqlens"], chunk_size=w.chunk_size, use_qk_l2norm=w.use_qk_l2norm, out=outs)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    l0 = gdr.launch_count()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            call()
+        e1.record(s)
+        torch.cuda.synchronize()
+    if gdr.device_status() != 0:
+        raise RuntimeError(f"device status after the backward: {gdr.last_error()}")
+    ms = e0.elapsed_time(e1) / steps
+    flops = bwd_algorithmic_flops(w)
+    clocks = clk.summary()
+    sm_mhz = clocks.get("sm_max_mhz") or 2070.0
+    peak = fp32_alu_tflops(sm_mhz)
+    achieved = flops / (ms * 1e-3) / 1e12
+    return {"workload": w.name, "value": w.B * w.T / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms, "steps": steps,
+            "gpu_launches_per_step": (gdr.launch_count() - l0) / steps, "clocks": clocks,
+            "roofline": {"bound": "alu", "kernel": "whole backward", "achieved": achieved,
+                         "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "algorithmic_flops_per_step": flops,
+                         "peak_source": "FP32 FMA: 152 SMs x 128 lanes x 2 x max SM clock"}}
+
+
+def decode_measurement(gdr, steps: int, warmup: int = 3):
+    """One decode step (the per-token form) on 256 sequences x 1 token, state
+    updated in place; L2 is flushed between steps by a 256 MB write."""
+    w = wl.GDN_BF16_DECODE
+    x = {k: (None if t is None else t.cuda()) for k, t in wl.make_inputs(w).items()}
+    state = x["h0"].clone()
+    o = torch.empty(w.B, w.T, w.HV, w.V, dtype=w.dtype, device="cuda")
+    flush = torch.empty(64 << 20, dtype=torch.float32, device="cuda")
+    s = torch.cuda.current_stream()
+
+    def call():
+        gdr.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], h0=state, use_qk_l2norm=True, algo="recurrent",
+                out=o, final_state=state)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    l0 = gdr.launch_count()
+    ms = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        call()
+        e1.record(s)
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    if gdr.device_status() != 0:
+        raise RuntimeError(f"device status after decode: {gdr.last_error()}")
+    avg = statistics.mean(ms)
+    byt = algorithmic_bytes(w)
+    pk = peaks()
+    achieved = byt / (avg * 1e-3) / 1e9
+    return {"workload": w.name, "value": w.B * w.T / (avg * 1e-3), "unit": UNIT, "ms_per_step": avg,
+            "steps": steps, "gpu_launches_per_step": (gdr.launch_count() - l0) / steps,
+            "l2_flush": "256 MB write between steps",
+            "roofline": {"bound": "hbm", "kernel": "recurrent_fwd_kernel", "achieved": achieved,
+                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                         "algorithmic_bytes_per_launch": byt}}
+
+
 def run_ours(args, w, world, rank, local):
     import chunked_gated_delta_08_gb300 as gdr
     pk = peaks()
@@ -366,6 +464,12 @@ def run_ours(args, w, world, rank, local):
         tok_s, dt, desc = oracle_sample(w, x, max(1, min(cores, w.N * w.HV)), cores)
         cpu = {"value": tok_s / dt, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
 
+    bwd = decode = None
+    if rank == 0 and world == 1 and not args.no_bwd:
+        bwd = bwd_measurement(gdr, steps=max(1, min(args.steps, 5)))
+    if rank == 0 and world == 1 and not args.no_decode:
+        decode = decode_measurement(gdr, steps=max(3, min(args.steps, 20)))
+
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -374,7 +478,8 @@ def run_ours(args, w, world, rank, local):
                 "e2e": {"value": world * tokens / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h},
                 "gpu_launches": launches, "roofline": roofline, "roofline_spec": roofline_spec,
-                "cpu_baseline": cpu, "step_ms": {"min": min(step_ms), "median": statistics.median(step_ms)}}
+                "cpu_baseline": cpu, "step_ms": {"min": min(step_ms), "median": statistics.median(step_ms)},
+                "bwd": bwd, "decode": decode}
         print(json.dumps(line), flush=True)
 
 
@@ -387,6 +492,8 @@ def main():
     ap.add_argument("--workload", default=wl.GDN_BF16_LARGE.name, choices=sorted(wl.BY_NAME))
     ap.add_argument("--algo", default="auto", choices=["auto", "chunked", "fused"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-bwd", action="store_true", help="skip the backward measurement")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     w = wl.BY_NAME[args.workload]

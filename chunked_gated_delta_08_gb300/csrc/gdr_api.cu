@@ -69,7 +69,7 @@ int validate(const gdr_desc *d, int chunk_size, const int64_t *cu) {
   if (d->dtype != GDR_F32 && d->dtype != GDR_BF16) return set_error(GDR_ERR_DTYPE, "dtype must be GDR_F32 or GDR_BF16");
   if (d->gate != GDR_GATE_SCALAR && d->gate != GDR_GATE_PER_K)
     return set_error(GDR_ERR_DTYPE, "gate must be GDR_GATE_SCALAR or GDR_GATE_PER_K");
-  if (d->algo < GDR_ALGO_AUTO || d->algo > GDR_ALGO_FUSED) return set_error(GDR_ERR_DTYPE, "unknown algo");
+  if (d->algo < GDR_ALGO_AUTO || d->algo > GDR_ALGO_RECURRENT) return set_error(GDR_ERR_DTYPE, "unknown algo");
   if (d->flags != 0) return set_error(GDR_ERR_DTYPE, "flags must be 0");
   if (d->B < 0 || d->T < 0) return set_error(GDR_ERR_SHAPE, "B and T must be >= 0");
   if (d->H <= 0 || d->HV <= 0) return set_error(GDR_ERR_SHAPE, "H and HV must be >= 1");
@@ -151,6 +151,41 @@ int run_chunked(const gdr_desc &d, const void *q, const void *k, const void *v, 
   if (rc == GDR_OK) rc = launch_chunk_fwd_o(a);
   e = cudaFreeAsync(base, stream);
   if (rc == GDR_OK && e != cudaSuccess) rc = cuda_error(e, "cudaFreeAsync (chunked scratch)");
+  return rc;
+}
+
+// The per-token form; the varlen layout first runs the chunk index to
+// validate cu_seqlens (its offsets are the only scratch).
+int run_recurrent(const gdr_desc &d, const void *q, const void *k, const void *v, const float *g, const void *beta,
+                  const float *h0, const int64_t *cu, int C, int l2, void *o, float *ht, cudaStream_t stream) {
+  int dev, rc;
+  if ((rc = current_device(&dev)) != GDR_OK) return rc;
+  int *status = device_status_word(dev, &rc);
+  if (!status) return rc;
+  ChunkedArgs a{};
+  a.d = d;
+  a.C = C;
+  a.l2 = l2;
+  a.q = q; a.k = k; a.v = v; a.beta = beta; a.g = g; a.h0 = h0; a.cu = cu;
+  a.o = o;
+  a.ht = ht;
+  a.status = status;
+  a.stream = stream;
+  char *base = nullptr;
+  if (cu) {
+    cudaMemPool_t pool;
+    if ((rc = scratch_pool(dev, &pool)) != GDR_OK) return rc;
+    cudaError_t e = cudaMallocFromPoolAsync((void **)&base, sizeof(int64_t) * (size_t)(d.N + 1), pool, stream);
+    if (e != cudaSuccess) return cuda_error(e, "cudaMallocFromPoolAsync (recurrent scratch)");
+    a.chunk_offsets = (int64_t *)base;
+    a.nt_max = 0;
+    rc = launch_chunk_index(a);
+  }
+  if (rc == GDR_OK) rc = launch_recurrent_fwd(a);
+  if (base) {
+    cudaError_t e = cudaFreeAsync(base, stream);
+    if (rc == GDR_OK && e != cudaSuccess) rc = cuda_error(e, "cudaFreeAsync (recurrent scratch)");
+  }
   return rc;
 }
 
@@ -269,6 +304,8 @@ int gdr_fwd(const gdr_desc *desc, const void *q, const void *k, const void *v, c
     return set_error(GDR_ERR_NULLPTR, "q, k, v, g, beta and o must be non-NULL");
   const int l2 = use_qk_l2norm ? 1 : 0;
   cudaStream_t s = (cudaStream_t)stream;
+  if (d.algo == GDR_ALGO_RECURRENT || (d.algo == GDR_ALGO_AUTO && !cu_seqlens && d.T <= 16))
+    return run_recurrent(d, q, k, v, g, beta, h0, cu_seqlens, chunk_size, l2, o, ht, s);
   if (d.algo != GDR_ALGO_CHUNKED) {
     int dev;
     if ((rc = current_device(&dev)) != GDR_OK) return rc;

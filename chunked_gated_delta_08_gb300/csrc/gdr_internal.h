@@ -77,4 +77,8 @@ int launch_chunk_prepare(const ChunkedArgs &a);
 int launch_chunk_fwd_h(const ChunkedArgs &a);
 int launch_chunk_fwd_o(const ChunkedArgs &a);
 
+// The per-token form (gdr_recurrent.cu): reads q, k, v, g, beta, h0, cu,
+// chunk_offsets (varlen only, from launch_chunk_index), writes o and ht.
+int launch_recurrent_fwd(const ChunkedArgs &a);
+
 }  // namespace gdr

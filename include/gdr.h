@@ -63,7 +63,8 @@ typedef enum gdr_gate { GDR_GATE_SCALAR = 0, GDR_GATE_PER_K = 1 } gdr_gate;
 typedef enum gdr_algo {
   GDR_ALGO_AUTO = 0,     /* fused single pass where supported, else the chunked three-kernel form */
   GDR_ALGO_CHUNKED = 1,  /* chunk index -> prepare -> fwd_h -> fwd_o, fp32 CUDA-core arithmetic */
-  GDR_ALGO_FUSED = 2     /* one persistent pass per (sequence, value head), tcgen05 tensor cores */
+  GDR_ALGO_FUSED = 2,    /* one persistent pass per (sequence, value head), tcgen05 tensor cores */
+  GDR_ALGO_RECURRENT = 3 /* token by token, state in registers (decode and other short inputs) */
 } gdr_algo;
 
 typedef struct gdr_desc {
@@ -90,6 +91,11 @@ typedef struct gdr_desc {
  * Scratch (the chunked form's w, u, h, v_new) is taken stream-ordered from a
  * library-owned memory pool on `stream` and returned to it before the call's
  * work completes; the fused form needs none.
+ * GDR_ALGO_AUTO picks the recurrent form for dense inputs with T <= 16, then
+ * the fused form where it applies, else the chunked form.  The recurrent form
+ * (the coverage guide's fused_recurrent path, section 三) follows the
+ * per-token recurrence directly; with it, ht may alias h0 for in-place
+ * decode.
  */
 int gdr_fwd(const gdr_desc *desc, const void *q, const void *k, const void *v, const float *g,
             const void *beta, const float *h0, const int64_t *cu_seqlens, int chunk_size,

@@ -78,7 +78,12 @@ WORKLOADS = [GDN_FP32_SMALL, GDN_BF16_GVA_K60, GDN_BF16_VARLEN, GDN_BF16_LARGE, 
 GDN_BF16_PROFILE = Workload("gdn_bf16_B1_T32768_H32_K128", torch.bfloat16, B=1, T=32768, H=32, HV=32,
                             K=128, V=128, use_qk_l2norm=True, h0_scale=None)
 
-BY_NAME = {w.name: w for w in WORKLOADS + [GDN_BF16_PROFILE]}
+# A decode step for the per-token form: 256 sequences, one new token each,
+# state carried in h0 (read) and ht (written); not one of the five workloads.
+GDN_BF16_DECODE = Workload("gdn_bf16_decode_N256_T1_H32_K128", torch.bfloat16, B=256, T=1, H=32, HV=32, K=128,
+                           V=128, use_qk_l2norm=True, h0_scale=0.1)
+
+BY_NAME = {w.name: w for w in WORKLOADS + [GDN_BF16_PROFILE, GDN_BF16_DECODE]}
 
 
 def make_inputs(w: Workload, device="cpu", seed: int | None = None) -> dict:
