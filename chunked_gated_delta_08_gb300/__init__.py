@@ -36,6 +36,7 @@ GDR_ERR_UNSUPPORTED = -9
 
 GDR_F32, GDR_BF16 = 0, 1
 GDR_GATE_SCALAR, GDR_GATE_PER_K = 0, 1
+GDR_FLAG_BETA_LOGITS = 1
 ALGOS = {"auto": 0, "chunked": 1, "fused": 2, "recurrent": 3}
 
 EXPORTED = ["gdr_fwd", "gdr_bwd", "gdr_fwd_noalloc", "gdr_chunked_sizes_get", "gdr_chunk_index", "gdr_chunk_prepare", "gdr_chunk_fwd_h",
@@ -121,7 +122,7 @@ def _stream_ptr(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def make_desc(q, v, g, cu_seqlens=None, algo="auto") -> GdrDesc:
+def make_desc(q, v, g, cu_seqlens=None, algo="auto", beta_logits=False) -> GdrDesc:
     B, T, H, K = q.shape
     HV, V = v.shape[2], v.shape[3]
     N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else B
@@ -129,7 +130,7 @@ def make_desc(q, v, g, cu_seqlens=None, algo="auto") -> GdrDesc:
     if dt is None:
         raise GdrError(GDR_ERR_DTYPE, f"unsupported dtype {q.dtype}")
     gate = GDR_GATE_PER_K if g.dim() == 4 else GDR_GATE_SCALAR
-    return GdrDesc(B, T, H, HV, K, V, N, dt, gate, ALGOS[algo], 0)
+    return GdrDesc(B, T, H, HV, K, V, N, dt, gate, ALGOS[algo], GDR_FLAG_BETA_LOGITS if beta_logits else 0)
 
 
 def _require(t, name, dtype=None, shape=None):
@@ -165,10 +166,12 @@ def _check_inputs(q, k, v, g, beta, h0, cu_seqlens):
 
 
 def fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, chunk_size=64, use_qk_l2norm=False,
-        output_final_state=True, algo="auto", out=None, final_state=None, stream=None):
-    """Chunked gated delta rule forward; returns ``(o, ht)`` (ht None unless requested)."""
+        output_final_state=True, algo="auto", out=None, final_state=None, stream=None, beta_logits=False):
+    """Chunked gated delta rule forward; returns ``(o, ht)`` (ht None unless requested).
+
+    ``beta_logits``: beta holds logits and the kernels apply the sigmoid."""
     B, T, H, K, HV, V, N = _check_inputs(q, k, v, g, beta, h0, cu_seqlens)
-    desc = make_desc(q, v, g, cu_seqlens, algo)
+    desc = make_desc(q, v, g, cu_seqlens, algo, beta_logits)
     o = out if out is not None else torch.empty(B, T, HV, V, dtype=q.dtype, device=q.device)
     _require(o, "out", q.dtype, (B, T, HV, V))
     ht = None
@@ -184,18 +187,19 @@ def fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, chunk_size=64, use_qk_l2norm
 
 
 def bwd(q, k, v, g, beta, do, dht=None, h0=None, cu_seqlens=None, chunk_size=64, use_qk_l2norm=False,
-        out=None, stream=None):
+        out=None, stream=None, beta_logits=False):
     """Backward of ``fwd`` for L = sum(o * do) + sum(ht * dht).
 
     Returns ``(dq, dk, dv, dg, dbeta, dh0)``: dq, dk, dv, dbeta in the input
     dtype, dg (shaped like g) and dh0 ([N,HV,K,V]) in fp32.  ``dht`` None means
     zero.  ``out`` may give the six output tensors.  The forward's
-    intermediates are recomputed inside the call.
+    intermediates are recomputed inside the call.  With ``beta_logits`` the
+    gradient in dbeta is with respect to the logits.
     """
     B, T, H, K, HV, V, N = _check_inputs(q, k, v, g, beta, h0, cu_seqlens)
     _require(do, "do", q.dtype, (B, T, HV, V))
     _require(dht, "dht", torch.float32, (N, HV, K, V))
-    desc = make_desc(q, v, g, cu_seqlens, "chunked")
+    desc = make_desc(q, v, g, cu_seqlens, "chunked", beta_logits)
     if out is None:
         dq, dk = torch.empty_like(q), torch.empty_like(k)
         dv, dbeta = torch.empty_like(v), torch.empty_like(beta)

@@ -70,7 +70,7 @@ int validate(const gdr_desc *d, int chunk_size, const int64_t *cu) {
   if (d->gate != GDR_GATE_SCALAR && d->gate != GDR_GATE_PER_K)
     return set_error(GDR_ERR_DTYPE, "gate must be GDR_GATE_SCALAR or GDR_GATE_PER_K");
   if (d->algo < GDR_ALGO_AUTO || d->algo > GDR_ALGO_RECURRENT) return set_error(GDR_ERR_DTYPE, "unknown algo");
-  if (d->flags != 0) return set_error(GDR_ERR_DTYPE, "flags must be 0");
+  if (d->flags & ~GDR_FLAG_BETA_LOGITS) return set_error(GDR_ERR_DTYPE, "unknown bits in flags");
   if (d->B < 0 || d->T < 0) return set_error(GDR_ERR_SHAPE, "B and T must be >= 0");
   if (d->H <= 0 || d->HV <= 0) return set_error(GDR_ERR_SHAPE, "H and HV must be >= 1");
   if (d->HV % d->H != 0) return set_error(GDR_ERR_SHAPE, "HV must be a multiple of H");

@@ -413,8 +413,8 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
     const float *__restrict__ dvn, const float *__restrict__ dW, const float *__restrict__ u,
     const float *__restrict__ w, const float *__restrict__ gcum, const int64_t *__restrict__ cu,
     const int64_t *__restrict__ chunk_indices, int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V, int l2,
-    float *__restrict__ dka, const float *__restrict__ dga, Tin *__restrict__ dv, Tin *__restrict__ dbeta,
-    float *__restrict__ dg) {
+    int beta_logits, float *__restrict__ dka, const float *__restrict__ dga, Tin *__restrict__ dv,
+    Tin *__restrict__ dbeta, float *__restrict__ dg) {
   constexpr int MQ = C * kKmax / kThreads;
   constexpr int MP = C * C / kThreads;
   constexpr int PR = kThreads / C;
@@ -442,7 +442,7 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
   for (int i = warp; i < C; i += kWarps) load_row_normed(k, t0 + i, H, hq, K, i < Lc, l2, ks + i * K, lane);
   load_gamma<PER_K>(gcum, t0, Lc, C, HV, hv, K, gam, tid);
   for (int i = tid; i < C; i += kThreads) {
-    bet[i] = i < Lc ? to_f32(beta[(t0 + i) * HV + hv]) : 0.f;
+    bet[i] = i < Lc ? load_beta(beta, (t0 + i) * HV + hv, beta_logits) : 0.f;
     dbs[i] = 0.f;
     rowacc[i] = 0.f;
   }
@@ -618,7 +618,9 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
       dg[(t0 + i) * HV + hv] = run;
     }
   }
-  for (int i = tid; i < Lc; i += kThreads) dbeta[(t0 + i) * HV + hv] = from_f32<Tin>(dbs[i]);
+  // with logits, dL/dx = dL/dbeta * beta (1 - beta)
+  for (int i = tid; i < Lc; i += kThreads)
+    dbeta[(t0 + i) * HV + hv] = from_f32<Tin>(beta_logits ? dbs[i] * bet[i] * (1.f - bet[i]) : dbs[i]);
 }
 
 // --------------------------------------------------------------------------
@@ -770,7 +772,8 @@ int launch_bwd_wy(const BwdArgs &a) {
     if (rc != GDR_OK) return rc;
     kern<<<dim3((unsigned)f.nt_max, (unsigned)f.d.HV), kThreads, smem, f.stream>>>(
         (const Tin *)f.k, (const Tin *)f.v, (const Tin *)f.beta, a.dvn, a.dW, f.u, f.w, f.gcum, f.cu,
-        f.chunk_indices, f.d.T, f.d.H, f.d.HV, K, f.d.V, f.l2, a.dka, a.dga, (Tin *)a.dv, (Tin *)a.dbeta, a.dg);
+        f.chunk_indices, f.d.T, f.d.H, f.d.HV, K, f.d.V, f.l2, (f.d.flags & GDR_FLAG_BETA_LOGITS) ? 1 : 0, a.dka,
+        a.dga, (Tin *)a.dv, (Tin *)a.dbeta, a.dg);
     return after_launch("bwd_wy_kernel");
   });
 }

@@ -108,7 +108,7 @@ template <typename Tin, int C, bool PER_K>
 __global__ void __launch_bounds__(kThreads) prepare_kernel(
     const Tin *__restrict__ k, const Tin *__restrict__ v, const float *__restrict__ g,
     const Tin *__restrict__ beta, const int64_t *__restrict__ cu, const int64_t *__restrict__ chunk_indices,
-    int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V, int l2, float *__restrict__ gcum,
+    int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V, int l2, int beta_logits, float *__restrict__ gcum,
     float *__restrict__ w, float *__restrict__ u) {
   extern __shared__ float smem[];
   float *ks = smem;
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(
     const int64_t i = e / gw, d = e % gw;
     gam[e] = i < Lc ? g[((t0 + i) * HV + hv) * gw + d] : 0.f;
   }
-  for (int i = tid; i < C; i += kThreads) bet[i] = i < Lc ? to_f32(beta[(t0 + i) * HV + hv]) : 0.f;
+  for (int i = tid; i < C; i += kThreads) bet[i] = i < Lc ? load_beta(beta, (t0 + i) * HV + hv, beta_logits) : 0.f;
   __syncthreads();
   for (int64_t d = tid; d < gw; d += kThreads) {
     float s = 0.f;
@@ -401,8 +401,8 @@ static int prepare_t(const ChunkedArgs &a) {
     int rc = launch_checked(kern, grid, smem, a.stream, "prepare_kernel");
     if (rc == GDR_OK && a.nt_max > 0) {
       kern<<<grid, kThreads, smem, a.stream>>>((const Tin *)a.k, (const Tin *)a.v, a.g, (const Tin *)a.beta, a.cu,
-                                               a.chunk_indices, a.d.T, a.d.H, a.d.HV, K, V, a.l2, a.gcum, a.w,
-                                               a.u);
+                                               a.chunk_indices, a.d.T, a.d.H, a.d.HV, K, V, a.l2,
+                                               (a.d.flags & GDR_FLAG_BETA_LOGITS) ? 1 : 0, a.gcum, a.w, a.u);
       rc = check_launch("prepare_kernel");
     }
     return rc;

@@ -70,6 +70,14 @@ __device__ __forceinline__ void load_row_normed(const Tin *__restrict__ x, int64
   }
 }
 
+// beta as stored, or the logistic sigmoid of a stored logit (the "raw beta"
+// input of the coverage guide, section 三).
+template <typename Tin>
+__device__ __forceinline__ float load_beta(const Tin *beta, int64_t idx, int logits) {
+  const float x = to_f32(beta[idx]);
+  return logits ? 1.f / (1.f + expf(-x)) : x;
+}
+
 // Records the first problem seen by any kernel into the status word.
 __device__ __forceinline__ void raise_status(int *status, int code) {
   if (status) atomicCAS(status, 0, code);

@@ -117,6 +117,7 @@ struct FusedParams {
   int *status;
   int64_t T, N, H, HV;
   int l2;
+  int beta_logits;
   unsigned long long timeout_cycles;
 };
 
@@ -644,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int i = lane; i < C; i += 32) {
         S.gb[slot][0][i] = i < L ? p.g[(t0 + i) * p.HV + hv] : 0.f;
-        S.gb[slot][1][i] = i < L ? __bfloat162float(p.beta[(t0 + i) * p.HV + hv]) : 0.f;
+        S.gb[slot][1][i] = i < L ? load_beta(p.beta, (t0 + i) * p.HV + hv, p.beta_logits) : 0.f;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&S.full_qk[slot]));
@@ -820,6 +821,7 @@ int run_fused(const gdr_desc &d, const void *q, const void *k, const void *v, co
   fp.H = d.H;
   fp.HV = d.HV;
   fp.l2 = l2;
+  fp.beta_logits = (d.flags & GDR_FLAG_BETA_LOGITS) ? 1 : 0;
   fp.timeout_cycles = 1ull << 32;  // about two seconds at GB300 clocks
   cudaError_t e = cudaFuncSetAttribute(gdr_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(gdr_fused_kernel)");

@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(kRThreads) recurrent_fwd_kernel(
     const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v, const float *__restrict__ g,
     const Tin *__restrict__ beta, const float *h0, const int64_t *__restrict__ cu,
     const int64_t *__restrict__ chunk_offsets, int64_t N, int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V,
-    int l2, Tin *__restrict__ o, float *ht) {
+    int l2, int beta_logits, Tin *__restrict__ o, float *ht) {
   __shared__ float kq[2][256];  // normalized k, q of the current token
   __shared__ float dec[256];    // exp(g) per row (per-key gate) or [0] (scalar)
   __shared__ float red[2][4][kRCols];
@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(kRThreads) recurrent_fwd_kernel(
     } else if (tid == 64) {
       dec[0] = expf(g[t * HV + hv]);
     }
-    const float b = to_f32(beta[t * HV + hv]);
+    const float b = load_beta(beta, t * HV + hv, beta_logits);
     const float vj = colok ? to_f32(v[(t * HV + hv) * V + col]) : 0.f;
     __syncthreads();
     // S <- D S; partial S^T k
@@ -118,7 +118,8 @@ template <typename Tin, bool PER_K, int ROWS>
 void launch_with(const ChunkedArgs &a, dim3 grid) {
   recurrent_fwd_kernel<Tin, PER_K, ROWS><<<grid, kRThreads, 0, a.stream>>>(
       (const Tin *)a.q, (const Tin *)a.k, (const Tin *)a.v, a.g, (const Tin *)a.beta, a.h0, a.cu, a.chunk_offsets,
-      a.d.N, a.d.T, a.d.H, a.d.HV, a.d.K, a.d.V, a.l2, (Tin *)a.o, a.ht);
+      a.d.N, a.d.T, a.d.H, a.d.HV, a.d.K, a.d.V, a.l2, (a.d.flags & GDR_FLAG_BETA_LOGITS) ? 1 : 0, (Tin *)a.o,
+      a.ht);
 }
 
 template <typename Tin, bool PER_K>

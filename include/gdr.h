@@ -73,8 +73,16 @@ typedef struct gdr_desc {
   int32_t dtype;   /* gdr_dtype of q, k, v, beta, o */
   int32_t gate;    /* gdr_gate */
   int32_t algo;    /* gdr_algo */
-  int32_t flags;   /* reserved, must be 0 */
+  int32_t flags;   /* GDR_FLAG_* bits; other bits must be 0 */
 } gdr_desc;
+
+/*
+ * GDR_FLAG_BETA_LOGITS: beta holds logits x and every kernel uses
+ * sigmoid(x) = 1 / (1 + exp(-x)) in its place (the coverage guide, section 三,
+ * tests "raw beta" beside "beta after sigmoid").  gdr_bwd then returns
+ * dL/dx = dL/dbeta * beta (1 - beta) in dbeta.
+ */
+#define GDR_FLAG_BETA_LOGITS 1
 
 /*
  * gdr_fwd -- the chunked forward of the gated delta rule.

@@ -110,8 +110,12 @@ def chunk_index_ref(cu_seqlens, chunk_size: int):
     return np.array(pairs, dtype=np.int64).reshape(-1, 2), offsets
 
 
+def _sigmoid(x):
+    return 1.0 / (1.0 + np.exp(-x))
+
+
 def gdr_fwd_ref(q, k, v, g, beta, h0=None, cu_seqlens=None, use_qk_l2norm=False,
-                chunk_size=None, want_v_new=False, threads=0, lib=None):
+                chunk_size=None, want_v_new=False, threads=0, lib=None, beta_logits=False):
     """Per-token fp64 recurrence over whole inputs.
 
     Shapes: q, k [B,T,H,K]; v [B,T,HV,V]; g [B,T,HV] (scalar gate, GDN) or
@@ -120,9 +124,13 @@ def gdr_fwd_ref(q, k, v, g, beta, h0=None, cu_seqlens=None, use_qk_l2norm=False,
     ``o`` [B,T,HV,V], ``ht`` [N,HV,K,V], and when ``chunk_size`` is given
     ``h_chunks`` [NT,HV,K,V] (state entering each chunk), and when
     ``want_v_new`` the per-token write vectors ``v_new`` [B,T,HV,V].
+    With ``beta_logits`` the given beta are logits x and beta = 1/(1 + e^-x)
+    (the coverage guide's "raw beta" axis, section 三).
     """
     lib = lib or _load()
     q, k, v, g, beta, h0 = (_f64(x) for x in (q, k, v, g, beta, h0))
+    if beta_logits:
+        beta = np.ascontiguousarray(_sigmoid(beta))
     B, T, H, K = q.shape
     HV, V = v.shape[2], v.shape[3]
     gate_per_k = 1 if g.ndim == 4 else 0
@@ -156,16 +164,20 @@ def gdr_fwd_ref(q, k, v, g, beta, h0=None, cu_seqlens=None, use_qk_l2norm=False,
 
 
 def gdr_bwd_ref(q, k, v, g, beta, do, dht=None, h0=None, cu_seqlens=None, use_qk_l2norm=False,
-                threads=0, lib=None):
+                threads=0, lib=None, beta_logits=False):
     """Reverse recurrence of the per-token forward, fp64.
 
     For the loss L = sum(o * do) + sum(ht * dht), returns a dict of numpy fp64
     arrays ``dq``, ``dk`` [B,T,H,K], ``dv`` [B,T,HV,V], ``dg`` shaped like g,
     ``dbeta`` [B,T,HV] and ``dh0`` [N,HV,K,V].  Shapes and layouts of the
-    inputs are those of ``gdr_fwd_ref``; ``dht`` None means zero.
+    inputs are those of ``gdr_fwd_ref``; ``dht`` None means zero.  With
+    ``beta_logits`` beta = sigmoid(x) and ``dbeta`` is dL/dx = dL/dbeta *
+    beta (1 - beta), the chain rule through the logistic function.
     """
     lib = lib or _load()
     q, k, v, g, beta, h0, do, dht = (_f64(x) for x in (q, k, v, g, beta, h0, do, dht))
+    if beta_logits:
+        beta = np.ascontiguousarray(_sigmoid(beta))
     B, T, H, K = q.shape
     HV, V = v.shape[2], v.shape[3]
     gate_per_k = 1 if g.ndim == 4 else 0
@@ -184,6 +196,8 @@ def gdr_bwd_ref(q, k, v, g, beta, do, dht=None, h0=None, cu_seqlens=None, use_qk
                             _ptr(out["dbeta"]), _ptr(out["dh0"]), int(threads))
     if rc != 0:
         raise RuntimeError(f"oracle failed with status {rc}")
+    if beta_logits:
+        out["dbeta"] = out["dbeta"] * beta * (1.0 - beta)
     return out
 
 

@@ -23,22 +23,22 @@ from tests.oracle_checks import close, rand_case
 FD_TOL = 1e-6
 
 
-def _loss(fwd, case, do, dht, l2):
+def _loss(fwd, case, do, dht, l2, **kw):
     out = fwd(case["q"], case["k"], case["v"], case["g"], case["beta"], h0=case["h0"],
-              cu_seqlens=case["cu_seqlens"], use_qk_l2norm=l2)
+              cu_seqlens=case["cu_seqlens"], use_qk_l2norm=l2, **kw)
     return float(np.sum(out["o"] * do) + np.sum(out["ht"] * dht))
 
 
-def finite_difference(fwd, case, do, dht, l2, name, step=1e-6):
+def finite_difference(fwd, case, do, dht, l2, name, step=1e-6, **kw):
     x = case[name]
     grad = np.zeros_like(x)
     flat = x.reshape(-1)
     for i in range(flat.size):
         old = flat[i]
         flat[i] = old + step
-        lp = _loss(fwd, case, do, dht, l2)
+        lp = _loss(fwd, case, do, dht, l2, **kw)
         flat[i] = old - step
-        lm = _loss(fwd, case, do, dht, l2)
+        lm = _loss(fwd, case, do, dht, l2, **kw)
         flat[i] = old
         grad.reshape(-1)[i] = (lp - lm) / (2 * step)
     return grad
@@ -134,6 +134,19 @@ def check_bwd_kda_uniform_equals_gdn(bwd, fwd, rng):
     close(kda["dg"].sum(-1), gdn["dg"], 1e-12, "dg summed over channels")
 
 
-ALL_BWD_CHECKS = [check_bwd_fd_gdn, check_bwd_fd_kda_varlen, check_bwd_fd_no_norm,
+def check_bwd_fd_beta_logits(bwd, fwd, rng):
+    """beta given as logits: dbeta is the gradient with respect to the logits."""
+    case = rand_case(rng, 1, 9, 1, 2, 3, 4)
+    case["beta"] = rng.standard_normal(case["beta"].shape) * 2.0
+    do = rng.standard_normal((1, 9, 2, 4))
+    dht = rng.standard_normal((1, 2, 3, 4))
+    got = bwd(case["q"], case["k"], case["v"], case["g"], case["beta"], do, dht=dht, h0=case["h0"],
+              use_qk_l2norm=True, beta_logits=True)
+    for name, key in (("beta", "dbeta"), ("k", "dk")):
+        ref = finite_difference(fwd, case, do, dht, True, name, beta_logits=True)
+        close(got[key], ref, FD_TOL, f"{key} vs finite differences (beta logits)")
+
+
+ALL_BWD_CHECKS = [check_bwd_fd_beta_logits, check_bwd_fd_gdn, check_bwd_fd_kda_varlen, check_bwd_fd_no_norm,
                   check_bwd_closed_form_frozen_state, check_bwd_varlen_equals_separate,
                   check_bwd_kda_uniform_equals_gdn]

@@ -47,7 +47,7 @@ def test_invalid_chunk_size(gdr, cs):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(H=3, HV=4), -2), (dict(K=300), -2), (dict(V=0), -2), (dict(T=-1), -2), (dict(N=2), -2),
-    (dict(dtype=7), -3), (dict(gate=5), -3), (dict(algo=9), -3), (dict(flags=1), -3),
+    (dict(dtype=7), -3), (dict(gate=5), -3), (dict(algo=9), -3), (dict(flags=2), -3),
 ])
 def test_invalid_shapes(gdr, kw, code):
     assert _call(gdr, _desc(gdr, **kw)) == code
