@@ -494,9 +494,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward measurement")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
+    ap.add_argument("--mode", default="fwd", choices=["fwd", "bwd", "decode"],
+                    help="bwd / decode: run only that measurement and print it alone")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     w = wl.BY_NAME[args.workload]
+    if args.mode != "fwd":  # one measurement alone (used for the profiles); one GPU
+        import chunked_gated_delta_08_gb300 as gdr
+        fn = bwd_measurement if args.mode == "bwd" else decode_measurement
+        res = fn(gdr, steps=args.steps, warmup=args.warmup)
+        print(json.dumps({"mode": args.mode, **res}), flush=True)
+        return
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, w, world, rank)

@@ -27,7 +27,7 @@ constexpr int kRCols = 32;      // V columns per block
 constexpr int kRMaxRows = 64;   // rows per warp: K <= 256
 
 template <typename Tin, bool PER_K, int ROWS>
-__global__ void __launch_bounds__(kRThreads) recurrent_fwd_kernel(
+__global__ void __launch_bounds__(kRThreads, ROWS <= 32 ? 8 : 4) recurrent_fwd_kernel(
     const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v, const float *__restrict__ g,
     const Tin *__restrict__ beta, const float *h0, const int64_t *__restrict__ cu,
     const int64_t *__restrict__ chunk_offsets, int64_t N, int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V,
@@ -39,16 +39,15 @@ __global__ void __launch_bounds__(kRThreads) recurrent_fwd_kernel(
   const int64_t unit = blockIdx.x, n = unit / HV, hv = unit % HV, hq = hv / (HV / H);
   const int64_t col = (int64_t)blockIdx.y * kRCols + lane;
   const bool colok = col < V;
-  const int64_t r0 = (int64_t)warp * ROWS;
+  const int r0 = warp * ROWS;                     // first state row of this warp
+  const int nrow = (int)(K - r0 < ROWS ? (K - r0 > 0 ? K - r0 : 0) : ROWS);  // rows < K it holds
   if (chunk_offsets && chunk_offsets[N] < 0) return;  // cu_seqlens rejected by the chunk index
   const SeqRange sr = seq_range(cu, n, T);
+  const int64_t state_base = (unit * K + r0) * V + col;  // row r0 of this column
 
   float S[ROWS];
 #pragma unroll
-  for (int r = 0; r < ROWS; ++r) {
-    const int64_t d = r0 + r;
-    S[r] = (h0 && colok && d < K) ? h0[((unit * K) + d) * V + col] : 0.f;
-  }
+  for (int r = 0; r < ROWS; ++r) S[r] = (h0 && colok && r < nrow) ? h0[state_base + (int64_t)r * V] : 0.f;
 
   for (int64_t t = sr.bos; t < sr.eos; ++t) {
     // k, q of the token, normalized (warps 0 and 1); decay factors (warps 2, 3)
@@ -58,32 +57,32 @@ __global__ void __launch_bounds__(kRThreads) recurrent_fwd_kernel(
       float ss = 0.f;
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
-        const int64_t d = lane + 32 * m;
+        const int d = lane + 32 * m;
         r[m] = d < K ? to_f32(x[d]) : 0.f;
         ss = fmaf(r[m], r[m], ss);
       }
       const float sc = l2 ? rsqrtf(warp_sum(ss) + kL2Eps) : 1.f;
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
-        const int64_t d = lane + 32 * m;
+        const int d = lane + 32 * m;
         if (d < K) kq[warp][d] = r[m] * sc;
       }
     } else if (PER_K) {
-      for (int64_t d = tid - 64; d < K; d += 64) dec[d] = expf(g[(t * HV + hv) * K + d]);
+      for (int d = tid - 64; d < K; d += 64) dec[d] = expf(g[(t * HV + hv) * K + d]);
     } else if (tid == 64) {
       dec[0] = expf(g[t * HV + hv]);
     }
     const float b = load_beta(beta, t * HV + hv, beta_logits);
     const float vj = colok ? to_f32(v[(t * HV + hv) * V + col]) : 0.f;
     __syncthreads();
-    // S <- D S; partial S^T k
+    // S <- D S; partial S^T k  (rows past K hold zero and read zero k)
+    const float *kr = kq[0] + r0, *qr = kq[1] + r0, *dr = dec + (PER_K ? r0 : 0);
     float pk = 0.f;
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {
-      const int64_t d = r0 + r;
-      if (d < K) {
-        S[r] *= PER_K ? dec[d] : dec[0];
-        pk = fmaf(S[r], kq[0][d], pk);
+      if (r < nrow) {
+        S[r] *= PER_K ? dr[r] : dr[0];
+        pk = fmaf(S[r], kr[r], pk);
       }
     }
     red[0][warp][lane] = pk;
@@ -93,10 +92,9 @@ __global__ void __launch_bounds__(kRThreads) recurrent_fwd_kernel(
     float po = 0.f;
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {
-      const int64_t d = r0 + r;
-      if (d < K) {
-        S[r] = fmaf(kq[0][d], e, S[r]);
-        po = fmaf(S[r], kq[1][d], po);
+      if (r < nrow) {
+        S[r] = fmaf(kr[r], e, S[r]);
+        po = fmaf(S[r], qr[r], po);
       }
     }
     red[1][warp][lane] = po;
@@ -107,10 +105,8 @@ __global__ void __launch_bounds__(kRThreads) recurrent_fwd_kernel(
   }
   if (ht && colok) {
 #pragma unroll
-    for (int r = 0; r < ROWS; ++r) {
-      const int64_t d = r0 + r;
-      if (d < K) ht[((unit * K) + d) * V + col] = S[r];
-    }
+    for (int r = 0; r < ROWS; ++r)
+      if (r < nrow) ht[state_base + (int64_t)r * V] = S[r];
   }
 }
 
