@@ -15,8 +15,10 @@ device -> host copies of o and ht) every step.  ``--impl reference`` times the
 fp64 CPU oracle on a bounded sample of the same workload.  On one GPU the line
 also carries ``bwd``: the backward timed on the KDA varlen workload (lengths
 700/324/3072/12288, HV 32, K 128, V 256), against the FP32 CUDA-core peak;
-and ``decode``: one decode step of the per-token form (256 sequences x 1
-token, 32 heads, K = V = 128, state in place) against HBM bandwidth.
+``decode``: one decode step of the per-token form (256 sequences x 1 token,
+32 heads, K = V = 128, state in place) against HBM bandwidth; and ``split``:
+the intra-sequence split on one 32768-token fp32 sequence with 4 heads,
+beside the unsplit chunked form.
 """
 from __future__ import annotations
 
@@ -376,6 +378,41 @@ def decode_measurement(gdr, steps: int, warmup: int = 3):
                          "algorithmic_bytes_per_launch": byt}}
 
 
+def split_measurement(gdr, steps: int, warmup: int = 3):
+    """The intra-sequence split against the unsplit chunked form on one long
+    sequence with four heads (fp32), inputs resident, CUDA events."""
+    w = wl.GDN_FP32_LONG_FEW
+    x = {k: (None if t is None else t.cuda()) for k, t in wl.make_inputs(w).items()}
+    s = torch.cuda.current_stream()
+    res = {}
+    for algo in ("split", "chunked"):
+        def call():
+            gdr.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], h0=x["h0"], use_qk_l2norm=True, algo=algo)
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize()
+        l0 = gdr.launch_count()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            call()
+        e1.record(s)
+        torch.cuda.synchronize()
+        res[algo] = (e0.elapsed_time(e1) / steps, (gdr.launch_count() - l0) / steps)
+    if gdr.device_status() != 0:
+        raise RuntimeError(f"device status after split: {gdr.last_error()}")
+    ms, launches = res["split"]
+    byt = algorithmic_bytes(w)
+    pk = peaks()
+    achieved = byt / (ms * 1e-3) / 1e9
+    return {"workload": w.name, "value": w.B * w.T / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
+            "steps": steps, "gpu_launches_per_step": launches, "chunked_ms_per_step": res["chunked"][0],
+            "speedup_vs_chunked": res["chunked"][0] / ms,
+            "roofline": {"bound": "hbm", "kernel": "whole split forward", "achieved": achieved,
+                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                         "algorithmic_bytes_per_launch": byt}}
+
+
 def run_ours(args, w, world, rank, local):
     import chunked_gated_delta_08_gb300 as gdr
     pk = peaks()
@@ -469,6 +506,9 @@ def run_ours(args, w, world, rank, local):
         bwd = bwd_measurement(gdr, steps=max(1, min(args.steps, 5)))
     if rank == 0 and world == 1 and not args.no_decode:
         decode = decode_measurement(gdr, steps=max(3, min(args.steps, 20)))
+    split = None
+    if rank == 0 and world == 1 and not args.no_split:
+        split = split_measurement(gdr, steps=max(1, min(args.steps, 3)))
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -479,7 +519,7 @@ def run_ours(args, w, world, rank, local):
                         "d2h_bytes_per_step": d2h},
                 "gpu_launches": launches, "roofline": roofline, "roofline_spec": roofline_spec,
                 "cpu_baseline": cpu, "step_ms": {"min": min(step_ms), "median": statistics.median(step_ms)},
-                "bwd": bwd, "decode": decode}
+                "bwd": bwd, "decode": decode, "split": split}
         print(json.dumps(line), flush=True)
 
 
@@ -494,14 +534,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward measurement")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
-    ap.add_argument("--mode", default="fwd", choices=["fwd", "bwd", "decode"],
+    ap.add_argument("--no-split", action="store_true", help="skip the intra-sequence split measurement")
+    ap.add_argument("--mode", default="fwd", choices=["fwd", "bwd", "decode", "split"],
                     help="bwd / decode: run only that measurement and print it alone")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     w = wl.BY_NAME[args.workload]
     if args.mode != "fwd":  # one measurement alone (used for the profiles); one GPU
         import chunked_gated_delta_08_gb300 as gdr
-        fn = bwd_measurement if args.mode == "bwd" else decode_measurement
+        fn = {"bwd": bwd_measurement, "decode": decode_measurement, "split": split_measurement}[args.mode]
         res = fn(gdr, steps=args.steps, warmup=args.warmup)
         print(json.dumps({"mode": args.mode, **res}), flush=True)
         return

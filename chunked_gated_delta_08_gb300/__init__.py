@@ -37,7 +37,7 @@ GDR_ERR_UNSUPPORTED = -9
 GDR_F32, GDR_BF16 = 0, 1
 GDR_GATE_SCALAR, GDR_GATE_PER_K = 0, 1
 GDR_FLAG_BETA_LOGITS = 1
-ALGOS = {"auto": 0, "chunked": 1, "fused": 2, "recurrent": 3}
+ALGOS = {"auto": 0, "chunked": 1, "fused": 2, "recurrent": 3, "split": 4}
 
 EXPORTED = ["gdr_fwd", "gdr_bwd", "gdr_fwd_noalloc", "gdr_chunked_sizes_get", "gdr_chunk_index", "gdr_chunk_prepare", "gdr_chunk_fwd_h",
             "gdr_chunk_fwd_o", "gdr_device_status", "gdr_last_error", "gdr_launch_count", "gdr_version"]

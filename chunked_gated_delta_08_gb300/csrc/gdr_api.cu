@@ -69,7 +69,7 @@ int validate(const gdr_desc *d, int chunk_size, const int64_t *cu) {
   if (d->dtype != GDR_F32 && d->dtype != GDR_BF16) return set_error(GDR_ERR_DTYPE, "dtype must be GDR_F32 or GDR_BF16");
   if (d->gate != GDR_GATE_SCALAR && d->gate != GDR_GATE_PER_K)
     return set_error(GDR_ERR_DTYPE, "gate must be GDR_GATE_SCALAR or GDR_GATE_PER_K");
-  if (d->algo < GDR_ALGO_AUTO || d->algo > GDR_ALGO_RECURRENT) return set_error(GDR_ERR_DTYPE, "unknown algo");
+  if (d->algo < GDR_ALGO_AUTO || d->algo > GDR_ALGO_SPLIT) return set_error(GDR_ERR_DTYPE, "unknown algo");
   if (d->flags & ~GDR_FLAG_BETA_LOGITS) return set_error(GDR_ERR_DTYPE, "unknown bits in flags");
   if (d->B < 0 || d->T < 0) return set_error(GDR_ERR_SHAPE, "B and T must be >= 0");
   if (d->H <= 0 || d->HV <= 0) return set_error(GDR_ERR_SHAPE, "H and HV must be >= 1");
@@ -151,6 +151,83 @@ int run_chunked(const gdr_desc &d, const void *q, const void *k, const void *v, 
   if (rc == GDR_OK) rc = launch_chunk_fwd_o(a);
   e = cudaFreeAsync(base, stream);
   if (rc == GDR_OK && e != cudaSuccess) rc = cuda_error(e, "cudaFreeAsync (chunked scratch)");
+  return rc;
+}
+
+// The chunked form with the state scan split into segments of kSplitTokens
+// tokens: prepare, segment transitions, merge, segment rescans, fwd_o.
+constexpr int kSplitTokens = 1024;
+
+int run_split(const gdr_desc &d, const void *q, const void *k, const void *v, const float *g, const void *beta,
+              const float *h0, const int64_t *cu, int C, int l2, void *o, float *ht, cudaStream_t stream) {
+  int dev, rc;
+  if ((rc = current_device(&dev)) != GDR_OK) return rc;
+  int *status = device_status_word(dev, &rc);
+  if (!status) return rc;
+  cudaMemPool_t pool;
+  if ((rc = scratch_pool(dev, &pool)) != GDR_OK) return rc;
+  gdr_chunked_sizes s;
+  sizes_of(d, C, cu, &s);
+  const int S = kSplitTokens / C;
+  const int64_t nseg_max = nt_max_of(d, S * C, cu);
+  const size_t sz[10] = {s.chunk_indices_bytes, s.chunk_offsets_bytes, s.gcum_bytes, s.w_bytes, s.u_bytes,
+                         s.v_new_bytes, s.h_bytes, sizeof(int64_t) * 2 * (size_t)nseg_max,
+                         sizeof(int64_t) * (size_t)(d.N + 1), 0};
+  const size_t x_bytes = sizeof(float) * (size_t)(nseg_max * d.HV * d.K * (d.V + d.K));
+  const size_t sin_bytes = sizeof(float) * (size_t)(nseg_max * d.HV * d.K * d.V);
+  size_t total = align256(x_bytes) + align256(sin_bytes);
+  for (size_t x : sz) total += align256(x);
+  char *base = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync((void **)&base, total > 0 ? total : 256, pool, stream);
+  if (e != cudaSuccess) return cuda_error(e, "cudaMallocFromPoolAsync (split scratch)");
+  char *ptr[9];
+  char *p = base;
+  for (int i = 0; i < 9; ++i) {
+    ptr[i] = p;
+    p += align256(sz[i]);
+  }
+  ChunkedArgs a{};
+  a.d = d;
+  a.C = C;
+  a.l2 = l2;
+  a.q = q; a.k = k; a.v = v; a.beta = beta; a.g = g; a.h0 = h0; a.cu = cu;
+  a.chunk_indices = cu ? (int64_t *)ptr[0] : nullptr;
+  a.chunk_offsets = cu ? (int64_t *)ptr[1] : nullptr;
+  a.gcum = (float *)ptr[2];
+  a.w = (float *)ptr[3];
+  a.u = (float *)ptr[4];
+  a.v_new = (float *)ptr[5];
+  a.h = (float *)ptr[6];
+  a.ht = ht;
+  a.o = o;
+  a.nt_max = s.nt_max;
+  a.status = status;
+  a.stream = stream;
+  SplitArgs sp{};
+  sp.S = S;
+  sp.nseg_max = nseg_max;
+  sp.seg_indices = cu ? (int64_t *)ptr[7] : nullptr;
+  sp.seg_offsets = cu ? (int64_t *)ptr[8] : nullptr;
+  sp.X = (float *)p;
+  sp.s_in = (float *)(p + align256(x_bytes));
+  if (cu) {
+    rc = launch_chunk_index(a);
+    if (rc == GDR_OK) {  // the same index over segments (chunks of S*C tokens)
+      ChunkedArgs sa = a;
+      sa.C = S * C;
+      sa.nt_max = nseg_max;
+      sa.chunk_indices = sp.seg_indices;
+      sa.chunk_offsets = sp.seg_offsets;
+      rc = launch_chunk_index(sa);
+    }
+  }
+  if (rc == GDR_OK) rc = launch_chunk_prepare(a);
+  if (rc == GDR_OK) rc = launch_split_transitions(a, sp);
+  if (rc == GDR_OK) rc = launch_split_merge(a, sp);
+  if (rc == GDR_OK) rc = launch_split_final(a, sp);
+  if (rc == GDR_OK) rc = launch_chunk_fwd_o(a);
+  e = cudaFreeAsync(base, stream);
+  if (rc == GDR_OK && e != cudaSuccess) rc = cuda_error(e, "cudaFreeAsync (split scratch)");
   return rc;
 }
 
@@ -306,6 +383,7 @@ int gdr_fwd(const gdr_desc *desc, const void *q, const void *k, const void *v, c
   cudaStream_t s = (cudaStream_t)stream;
   if (d.algo == GDR_ALGO_RECURRENT || (d.algo == GDR_ALGO_AUTO && !cu_seqlens && d.T <= 16))
     return run_recurrent(d, q, k, v, g, beta, h0, cu_seqlens, chunk_size, l2, o, ht, s);
+  if (d.algo == GDR_ALGO_SPLIT) return run_split(d, q, k, v, g, beta, h0, cu_seqlens, chunk_size, l2, o, ht, s);
   if (d.algo != GDR_ALGO_CHUNKED) {
     int dev;
     if ((rc = current_device(&dev)) != GDR_OK) return rc;
@@ -316,6 +394,9 @@ int gdr_fwd(const gdr_desc *desc, const void *q, const void *k, const void *v, c
       if (rc == GDR_ERR_UNSUPPORTED) set_error(rc, "the fused form does not support this request");
       return rc;
     }
+    // dense, long, and too few state-scan blocks to fill the GPU: split the scan
+    if (!cu_seqlens && d.T >= 4 * kSplitTokens && d.N * d.HV * cdiv(d.V, 32) < 152)
+      return run_split(d, q, k, v, g, beta, h0, cu_seqlens, chunk_size, l2, o, ht, s);
   }
   return run_chunked(d, q, k, v, g, beta, h0, cu_seqlens, chunk_size, l2, o, ht, s);
 }

@@ -77,6 +77,20 @@ int launch_chunk_prepare(const ChunkedArgs &a);
 int launch_chunk_fwd_h(const ChunkedArgs &a);
 int launch_chunk_fwd_o(const ChunkedArgs &a);
 
+// The intra-sequence split of the state scan (gdr_split.cu).  Segments are
+// S chunks long; seg_indices / seg_offsets are the chunk index built with a
+// chunk length of S*C tokens (varlen only).
+struct SplitArgs {
+  int S;
+  int64_t nseg_max;
+  int64_t *seg_indices, *seg_offsets;
+  float *X;     // [nseg_max, HV, K, V + K]: [S_ext | M] per segment
+  float *s_in;  // [nseg_max, HV, K, V]: state entering each segment
+};
+int launch_split_transitions(const ChunkedArgs &a, const SplitArgs &sp);
+int launch_split_merge(const ChunkedArgs &a, const SplitArgs &sp);
+int launch_split_final(const ChunkedArgs &a, const SplitArgs &sp);
+
 // The per-token form (gdr_recurrent.cu): reads q, k, v, g, beta, h0, cu,
 // chunk_offsets (varlen only, from launch_chunk_index), writes o and ht.
 int launch_recurrent_fwd(const ChunkedArgs &a);

@@ -64,7 +64,8 @@ typedef enum gdr_algo {
   GDR_ALGO_AUTO = 0,     /* fused single pass where supported, else the chunked three-kernel form */
   GDR_ALGO_CHUNKED = 1,  /* chunk index -> prepare -> fwd_h -> fwd_o, fp32 CUDA-core arithmetic */
   GDR_ALGO_FUSED = 2,    /* one persistent pass per (sequence, value head), tcgen05 tensor cores */
-  GDR_ALGO_RECURRENT = 3 /* token by token, state in registers (decode and other short inputs) */
+  GDR_ALGO_RECURRENT = 3, /* token by token, state in registers (decode and other short inputs) */
+  GDR_ALGO_SPLIT = 4      /* chunked, state scan split into 1024-token segments merged by transitions */
 } gdr_algo;
 
 typedef struct gdr_desc {
@@ -103,7 +104,13 @@ typedef struct gdr_desc {
  * the fused form where it applies, else the chunked form.  The recurrent form
  * (the coverage guide's fused_recurrent path, section 三) follows the
  * per-token recurrence directly; with it, ht may alias h0 for in-place
- * decode.
+ * decode.  GDR_ALGO_SPLIT is the chunked form with the state scan split
+ * inside each sequence (the KCP handbook's segment transition M and end
+ * state S_ext, merged on one GPU): segments of 1024 tokens run in parallel,
+ * for inputs with few (sequence, value head) pairs and long sequences.
+ * AUTO takes it when the fused form does not apply, the input is dense with
+ * T >= 4096, and N * HV * ceil(V / 32) < 152 (fewer state-scan blocks than
+ * the GPU has SMs).
  */
 int gdr_fwd(const gdr_desc *desc, const void *q, const void *k, const void *v, const float *g,
             const void *beta, const float *h0, const int64_t *cu_seqlens, int chunk_size,

@@ -83,7 +83,12 @@ GDN_BF16_PROFILE = Workload("gdn_bf16_B1_T32768_H32_K128", torch.bfloat16, B=1, 
 GDN_BF16_DECODE = Workload("gdn_bf16_decode_N256_T1_H32_K128", torch.bfloat16, B=256, T=1, H=32, HV=32, K=128,
                            V=128, use_qk_l2norm=True, h0_scale=0.1)
 
-BY_NAME = {w.name: w for w in WORKLOADS + [GDN_BF16_PROFILE, GDN_BF16_DECODE]}
+# Few (sequence, head) units and a long sequence, fp32 (the chunked family):
+# the case the intra-sequence split is for; not one of the five workloads.
+GDN_FP32_LONG_FEW = Workload("gdn_fp32_B1_T32768_H4_K128", torch.float32, B=1, T=32768, H=4, HV=4, K=128, V=128,
+                             use_qk_l2norm=True, h0_scale=0.1)
+
+BY_NAME = {w.name: w for w in WORKLOADS + [GDN_BF16_PROFILE, GDN_BF16_DECODE, GDN_FP32_LONG_FEW]}
 
 
 def make_inputs(w: Workload, device="cpu", seed: int | None = None) -> dict:
