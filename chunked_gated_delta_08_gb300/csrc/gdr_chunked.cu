@@ -9,7 +9,8 @@
 //                       forward substitution to give w and u
 //   fwd_h_kernel        per (sequence, value head, V-tile), sequential over
 //                       chunks: h (state entering the chunk), v_new = u - w h,
-//                       h <- exp(G_C) h + (K * exp(G_C - G))^T v_new
+//                       h <- exp(G_C) h + (K * exp(G_C - G))^T v_new, both
+//                       products on tensor cores in 3 x TF32 (gdr_scan.cuh)
 //   fwd_o_kernel        per (chunk, value head): o = (q * exp G) h + P v_new
 //                       with P = tril(q k^T * decay) (diagonal included)
 //
@@ -20,6 +21,7 @@
 
 #include "gdr_device.cuh"
 #include "gdr_internal.h"
+#include "gdr_scan.cuh"
 
 namespace gdr {
 namespace {
@@ -194,7 +196,7 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(
 
 // --------------------------------------------------------------------------
 // fwd_h: grid (N, HV, ceil(V / 32)), sequential over the sequence's chunks.
-// smem: hs[K*32] | ws[C*K] | kt[C*K] | vn[C*32] | gl[K]
+// Each chunk's two products run on tensor cores in 3 x TF32 (gdr_scan.cuh).
 // --------------------------------------------------------------------------
 template <typename Tin, int C, bool PER_K>
 __global__ void __launch_bounds__(kThreads) fwd_h_kernel(
@@ -203,22 +205,19 @@ __global__ void __launch_bounds__(kThreads) fwd_h_kernel(
     const int64_t *__restrict__ chunk_offsets, int64_t N, int64_t T, int64_t H, int64_t HV, int64_t K,
     int64_t V, int l2, float *__restrict__ h, float *__restrict__ v_new, float *__restrict__ ht) {
   extern __shared__ float smem[];
-  float *hs = smem;
-  float *ws = hs + K * kBVh;
-  float *kt = ws + C * K;
-  float *vn = kt + C * K;
-  float *gl = vn + C * kBVh;
+  const scan::Tiles st = scan::carve(smem, C, K);
   if (chunk_offsets && chunk_offsets[N] < 0) return;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int64_t n = blockIdx.x, hv = blockIdx.y, v0 = (int64_t)blockIdx.z * kBVh;
   const int64_t hq = hv / (HV / H);
+  const int64_t Kp = scan::kpad(K);
   const SeqRange sr = seq_range(cu, n, T);
   const int64_t nch = (sr.eos - sr.bos + C - 1) / C;
   const int64_t cbase = chunk_offsets ? chunk_offsets[n] : n * ((T + C - 1) / C);
 
-  for (int64_t e = tid; e < K * kBVh; e += kThreads) {
+  for (int64_t e = tid; e < Kp * kBVh; e += kThreads) {
     const int64_t d = e / kBVh, vv = e % kBVh;
-    hs[e] = (h0 && v0 + vv < V) ? h0[((n * HV + hv) * K + d) * V + v0 + vv] : 0.f;
+    st.hs[d * scan::kHS + vv] = (h0 && d < K && v0 + vv < V) ? h0[((n * HV + hv) * K + d) * V + v0 + vv] : 0.f;
   }
   __syncthreads();
 
@@ -228,46 +227,14 @@ __global__ void __launch_bounds__(kThreads) fwd_h_kernel(
     if (h)
       for (int64_t e = tid; e < K * kBVh; e += kThreads) {
         const int64_t d = e / kBVh, vv = e % kBVh;
-        if (v0 + vv < V) h[(((cbase + c) * HV + hv) * K + d) * V + v0 + vv] = hs[e];
+        if (v0 + vv < V) h[(((cbase + c) * HV + hv) * K + d) * V + v0 + vv] = st.hs[d * scan::kHS + vv];
       }
-    const int64_t tl = t0 + Lc - 1;  // last valid token of the chunk
-    for (int64_t d = tid; d < K; d += kThreads)
-      gl[d] = PER_K ? gcum[(tl * HV + hv) * K + d] : gcum[tl * HV + hv];
-    __syncthreads();
-    for (int i = warp; i < C; i += kWarps) {
-      load_row_normed(k, t0 + i, H, hq, K, i < Lc, l2, kt + i * K, lane);
-      for (int64_t d = lane; d < K; d += 32) {
-        const float gi = i < Lc ? (PER_K ? gcum[((t0 + i) * HV + hv) * K + d] : gcum[(t0 + i) * HV + hv]) : 0.f;
-        kt[i * K + d] *= (i < Lc) ? expf(gl[d] - gi) : 0.f;
-        ws[i * K + d] = i < Lc ? w[((t0 + i) * HV + hv) * K + d] : 0.f;
-      }
-    }
-    __syncthreads();
-    // v_new = u - w h
-    for (int64_t e = tid; e < C * kBVh; e += kThreads) {
-      const int i = (int)(e / kBVh), vv = (int)(e % kBVh);
-      float acc = 0.f;
-      if (i < Lc && v0 + vv < V) {
-        acc = u[((t0 + i) * HV + hv) * V + v0 + vv];
-        for (int64_t d = 0; d < K; ++d) acc = fmaf(-ws[i * K + d], hs[d * kBVh + vv], acc);
-        if (v_new) v_new[((t0 + i) * HV + hv) * V + v0 + vv] = acc;
-      }
-      vn[e] = acc;
-    }
-    __syncthreads();
-    // h <- exp(G_C) h + (K * exp(G_C - G))^T v_new
-    for (int64_t e = tid; e < K * kBVh; e += kThreads) {
-      const int64_t d = e / kBVh, vv = e % kBVh;
-      float acc = hs[e] * expf(gl[d]);
-      for (int i = 0; i < Lc; ++i) acc = fmaf(kt[i * K + d], vn[i * kBVh + vv], acc);
-      hs[e] = acc;
-    }
-    __syncthreads();
+    scan::chunk_step<Tin, C, PER_K>(st, k, w, u, gcum, t0, Lc, hv, hq, H, HV, K, V, V, v0, l2, v_new);
   }
   if (ht)
     for (int64_t e = tid; e < K * kBVh; e += kThreads) {
       const int64_t d = e / kBVh, vv = e % kBVh;
-      if (v0 + vv < V) ht[((n * HV + hv) * K + d) * V + v0 + vv] = hs[e];
+      if (v0 + vv < V) ht[((n * HV + hv) * K + d) * V + v0 + vv] = st.hs[d * scan::kHS + vv];
     }
 }
 
@@ -415,7 +382,7 @@ static int fwd_h_t(const ChunkedArgs &a) {
   return dispatch_cfg(a.C, a.d.gate == GDR_GATE_PER_K, [&](auto cfg) {
     constexpr int CC = decltype(cfg)::C;
     constexpr bool PK = decltype(cfg)::PK;
-    const size_t smem = sizeof(float) * (K * kBVh + 2 * CC * K + CC * kBVh + K);
+    const size_t smem = sizeof(float) * scan::smem_floats(CC, K);
     auto kern = fwd_h_kernel<Tin, CC, PK>;
     dim3 grid((unsigned)a.d.N, (unsigned)a.d.HV, (unsigned)cdiv(V, kBVh));
     int rc = launch_checked(kern, grid, smem, a.stream, "fwd_h_kernel");

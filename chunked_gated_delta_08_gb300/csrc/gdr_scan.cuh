@@ -1,0 +1,176 @@
+// gdr_scan.cuh -- one chunk of the state scan on a 32-column tile, with both
+// of its products on warp-level tensor-core MMAs in 3 x TF32 (close to fp32).
+//
+// For the chunk starting at token t0 with Lc valid rows, h the K x 32 state
+// tile entering it (shared memory), Gamma the gate cumsum and L the last
+// valid row:
+//   v_new = u - w h                    (C x 32)  = (C x K)(K x 32)
+//   h    <- e^{G_L} h + Kb^T v_new      (K x 32)  = (K x C)(C x 32),  Kb = k e^{G_L - G}
+// (the chunk form of the recurrence; the KCP handbook's h is the state
+// entering the chunk).  Columns at or past `ucols` take u = 0 (the
+// transition columns of the intra-sequence split).
+//
+// Shared-memory tiles, padded so every fragment load is free of bank
+// conflicts (Kp = K rounded up to 16):
+//   hs [Kp][kHS]   state tile          ws [C][Kp + 4]  -w
+//   kt [C][Kp + 8] Kb                  vn [C][kHS]     v_new
+//   gl [Kp]        G_L per key row
+#pragma once
+
+#include "gdr_device.cuh"
+#include "gdr_sm100.cuh"
+
+namespace gdr {
+namespace scan {
+
+constexpr int kCols = 32;      // columns of the state tile
+constexpr int kHS = kCols + 8; // row stride of hs and vn (== 8 mod 32)
+constexpr int kScanThreads = 256;
+
+__host__ __device__ constexpr int64_t kpad(int64_t K) { return (K + 15) / 16 * 16; }
+__host__ __device__ constexpr int64_t ws_ld(int64_t K) { return kpad(K) + 4; }
+__host__ __device__ constexpr int64_t kt_ld(int64_t K) { return kpad(K) + 8; }
+
+// floats of shared memory the tiles need
+__host__ __device__ constexpr int64_t smem_floats(int C, int64_t K) {
+  return kpad(K) * kHS + C * ws_ld(K) + C * kt_ld(K) + C * kHS + kpad(K);
+}
+
+struct Tiles {
+  float *hs, *ws, *kt, *vn, *gl;
+};
+
+__device__ __forceinline__ Tiles carve(float *smem, int C, int64_t K) {
+  Tiles t;
+  t.hs = smem;
+  t.ws = t.hs + kpad(K) * kHS;
+  t.kt = t.ws + C * ws_ld(K);
+  t.vn = t.kt + C * kt_ld(K);
+  t.gl = t.vn + C * kHS;
+  return t;
+}
+
+__device__ __forceinline__ void split3(float x, uint32_t &hi, uint32_t &lo) { sm100::split_tf32(x, hi, lo); }
+
+// d += A B with A, B split into (hi, lo); the lo * lo term is dropped.
+__device__ __forceinline__ void mma3(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4],
+                                     const uint32_t (&bh)[2], const uint32_t (&bl)[2]) {
+  sm100::mma_tf32(d, al[0], al[1], al[2], al[3], bh[0], bh[1]);
+  sm100::mma_tf32(d, ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
+  sm100::mma_tf32(d, ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
+}
+
+// One chunk.  Called by all 256 threads of the block; hs holds the entering
+// tile and holds the leaving one on return.  v_new_out (nullable) receives
+// v_new for rows < Lc and columns < ucols.  c0col is the tile's first column
+// in the scanned matrix.
+template <typename Tin, int C, bool PER_K>
+__device__ __forceinline__ void chunk_step(const Tiles &s, const Tin *__restrict__ k, const float *__restrict__ w,
+                                           const float *__restrict__ u, const float *__restrict__ gcum,
+                                           int64_t t0, int Lc, int64_t hv, int64_t hq, int64_t H, int64_t HV,
+                                           int64_t K, int64_t V, int64_t ucols, int64_t c0col, int l2,
+                                           float *__restrict__ v_new_out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, tq = lane & 3;
+  const int64_t Kp = kpad(K), WL = ws_ld(K), KL = kt_ld(K);
+  const int64_t gw = PER_K ? K : 1;
+  const int64_t tl = t0 + Lc - 1;
+  for (int64_t d = tid; d < Kp; d += kScanThreads)
+    s.gl[d] = d < K ? gcum[(tl * HV + hv) * gw + (PER_K ? d : 0)] : 0.f;
+  __syncthreads();
+  // Kb and -w, zero past Lc and past K
+  constexpr int kWarps = kScanThreads / 32;
+  for (int i = warp; i < C; i += kWarps) {
+    float *kr = s.kt + i * KL;
+    load_row_normed(k, t0 + i, H, hq, K, i < Lc, l2, kr, lane);
+    for (int64_t d = lane; d < Kp; d += 32) {
+      const bool ok = i < Lc && d < K;
+      const float gi = ok ? gcum[((t0 + i) * HV + hv) * gw + (PER_K ? d : 0)] : 0.f;
+      kr[d] = ok ? kr[d] * expf(s.gl[d] - gi) : 0.f;
+      s.ws[i * WL + d] = ok ? -w[((t0 + i) * HV + hv) * K + d] : 0.f;
+    }
+  }
+  __syncthreads();
+
+  // ---- v_new = u - w h: C x 32, warp -> rows 16 (warp & 3) .., columns 16 (warp >> 2) ..
+  if (warp < 2 * (C / 16)) {
+    const int m0 = 16 * (warp % (C / 16)), n0 = 16 * (warp / (C / 16));
+    float acc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = m0 + g + 8 * (e >> 1);
+        const int64_t col = c0col + n0 + 8 * nt + 2 * tq + (e & 1);
+        acc[nt][e] = (i < Lc && col < ucols) ? u[((t0 + i) * HV + hv) * V + col] : 0.f;
+      }
+    for (int64_t k0 = 0; k0 < Kp; k0 += 8) {
+      uint32_t ah[4], al[4];
+      const float *a = s.ws + (m0 + g) * WL + k0 + tq;
+      split3(a[0], ah[0], al[0]);
+      split3(a[8 * WL], ah[1], al[1]);
+      split3(a[4], ah[2], al[2]);
+      split3(a[8 * WL + 4], ah[3], al[3]);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const float *b = s.hs + (k0 + tq) * kHS + n0 + 8 * nt + g;
+        uint32_t bh[2], bl[2];
+        split3(b[0], bh[0], bl[0]);
+        split3(b[4 * kHS], bh[1], bl[1]);
+        mma3(acc[nt], ah, al, bh, bl);
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = m0 + g + 8 * (e >> 1);
+        const int cc = n0 + 8 * nt + 2 * tq + (e & 1);
+        s.vn[i * kHS + cc] = acc[nt][e];  // zero past Lc (w, u are zero there)
+        const int64_t col = c0col + cc;
+        if (v_new_out && i < Lc && col < ucols) v_new_out[((t0 + i) * HV + hv) * V + col] = acc[nt][e];
+      }
+  }
+  __syncthreads();
+
+  // ---- h <- e^{G_L} h + Kb^T v_new: Kp x 32, warp -> row tiles warp, warp + 8, ..., all 4 column tiles
+  for (int64_t m0 = 16 * warp; m0 < Kp; m0 += 16 * kWarps) {
+    float acc[4][4];
+    const float e0 = expf(s.gl[PER_K ? m0 + g : 0]), e1 = expf(s.gl[PER_K ? m0 + g + 8 : 0]);
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int64_t d = m0 + g + 8 * (e >> 1);
+        acc[nt][e] = s.hs[d * kHS + 8 * nt + 2 * tq + (e & 1)] * ((e >> 1) ? e1 : e0);
+      }
+#pragma unroll
+    for (int k0 = 0; k0 < C; k0 += 8) {
+      uint32_t ah[4], al[4];
+      const float *a = s.kt + (k0 + tq) * KL + m0 + g;  // A(d, i) = Kb[i][d]
+      split3(a[0], ah[0], al[0]);
+      split3(a[8], ah[1], al[1]);
+      split3(a[4 * KL], ah[2], al[2]);
+      split3(a[4 * KL + 8], ah[3], al[3]);
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const float *b = s.vn + (k0 + tq) * kHS + 8 * nt + g;
+        uint32_t bh[2], bl[2];
+        split3(b[0], bh[0], bl[0]);
+        split3(b[4 * kHS], bh[1], bl[1]);
+        mma3(acc[nt], ah, al, bh, bl);
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int64_t d = m0 + g + 8 * (e >> 1);
+        s.hs[d * kHS + 8 * nt + 2 * tq + (e & 1)] = acc[nt][e];
+      }
+  }
+  __syncthreads();
+}
+
+}  // namespace scan
+}  // namespace gdr

@@ -23,17 +23,17 @@
 // the state-scan arithmetic.
 #include "gdr_device.cuh"
 #include "gdr_internal.h"
+#include "gdr_scan.cuh"
 
 namespace gdr {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
 constexpr int kTile = 32;  // columns per block
 
 // FINAL = false: columns [0, V + K) of X = [S_ext | M], X starting at [0 | I].
 // FINAL = true:  columns [0, V) of the state, starting at S_in of the segment.
-// smem: hs[K*32] | ws[C*K] | kt[C*K] | vn[C*32] | gl[K]
+// Each chunk is one scan::chunk_step (tensor cores, 3 x TF32).
 template <typename Tin, int C, bool PER_K, bool FINAL>
 __global__ void __launch_bounds__(kThreads) seg_scan_kernel(
     const Tin *__restrict__ k, const float *__restrict__ w, const float *__restrict__ u,
@@ -42,32 +42,30 @@ __global__ void __launch_bounds__(kThreads) seg_scan_kernel(
     int l2, float *__restrict__ X, const float *__restrict__ s_in, float *__restrict__ h,
     float *__restrict__ v_new, float *__restrict__ ht) {
   extern __shared__ float smem[];
-  float *hs = smem;
-  float *ws = hs + K * kTile;
-  float *kt = ws + C * K;
-  float *vn = kt + C * K;
-  float *gl = vn + C * kTile;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const scan::Tiles st = scan::carve(smem, C, K);
+  const int tid = threadIdx.x;
   const int64_t seg = blockIdx.x, hv = blockIdx.y, c0col = (int64_t)blockIdx.z * kTile;
   const int64_t ncol = FINAL ? V : V + K;  // width of the scanned matrix
   const int64_t hq = hv / (HV / H);
+  const int64_t Kp = scan::kpad(K);
   int64_t n, s;
   if (!chunk_coords(seg_indices, seg, T, C * S, &n, &s)) return;
   const SeqRange sr = seq_range(cu, n, T);
   const int64_t nch = (sr.eos - sr.bos + C - 1) / C;
   const int64_t cbeg = s * S, cend = (cbeg + S < nch) ? cbeg + S : nch;
   const int64_t cbase = chunk_offsets ? chunk_offsets[n] : n * ((T + C - 1) / C);
-  const int64_t gw = PER_K ? K : 1;
 
-  for (int64_t e = tid; e < K * kTile; e += kThreads) {
+  for (int64_t e = tid; e < Kp * kTile; e += kThreads) {
     const int64_t d = e / kTile, col = c0col + e % kTile;
     float x = 0.f;
-    if (FINAL) {
-      if (col < V) x = s_in[((seg * HV + hv) * K + d) * V + col];
-    } else if (col >= V && col < ncol) {
-      x = (col - V == d) ? 1.f : 0.f;
+    if (d < K) {
+      if (FINAL) {
+        if (col < V) x = s_in[((seg * HV + hv) * K + d) * V + col];
+      } else if (col >= V && col < ncol) {
+        x = (col - V == d) ? 1.f : 0.f;
+      }
     }
-    hs[e] = x;
+    st.hs[d * scan::kHS + e % kTile] = x;
   }
   __syncthreads();
 
@@ -77,52 +75,21 @@ __global__ void __launch_bounds__(kThreads) seg_scan_kernel(
     if (FINAL && h)
       for (int64_t e = tid; e < K * kTile; e += kThreads) {
         const int64_t d = e / kTile, col = c0col + e % kTile;
-        if (col < V) h[(((cbase + c) * HV + hv) * K + d) * V + col] = hs[e];
+        if (col < V) h[(((cbase + c) * HV + hv) * K + d) * V + col] = st.hs[d * scan::kHS + e % kTile];
       }
-    const int64_t tl = t0 + Lc - 1;
-    for (int64_t d = tid; d < K; d += kThreads) gl[d] = gcum[(tl * HV + hv) * gw + (PER_K ? d : 0)];
-    __syncthreads();
-    for (int i = warp; i < C; i += kWarps) {
-      load_row_normed(k, t0 + i, H, hq, K, i < Lc, l2, kt + i * K, lane);
-      for (int64_t d = lane; d < K; d += 32) {
-        const float gi = i < Lc ? gcum[((t0 + i) * HV + hv) * gw + (PER_K ? d : 0)] : 0.f;
-        kt[i * K + d] *= (i < Lc) ? expf(gl[d] - gi) : 0.f;
-        ws[i * K + d] = i < Lc ? w[((t0 + i) * HV + hv) * K + d] : 0.f;
-      }
-    }
-    __syncthreads();
-    // v_new = u - w x  (u is zero in the M columns)
-    for (int64_t e = tid; e < C * kTile; e += kThreads) {
-      const int i = (int)(e / kTile), vv = (int)(e % kTile);
-      const int64_t col = c0col + vv;
-      float acc = 0.f;
-      if (i < Lc && col < ncol) {
-        acc = col < V ? u[((t0 + i) * HV + hv) * V + col] : 0.f;
-        for (int64_t d = 0; d < K; ++d) acc = fmaf(-ws[i * K + d], hs[d * kTile + vv], acc);
-        if (FINAL && v_new) v_new[((t0 + i) * HV + hv) * V + col] = acc;
-      }
-      vn[e] = acc;
-    }
-    __syncthreads();
-    // x <- exp(G_L) x + Kb^T v_new
-    for (int64_t e = tid; e < K * kTile; e += kThreads) {
-      const int64_t d = e / kTile, vv = e % kTile;
-      float acc = hs[e] * expf(gl[d]);
-      for (int i = 0; i < Lc; ++i) acc = fmaf(kt[i * K + d], vn[i * kTile + vv], acc);
-      hs[e] = acc;
-    }
-    __syncthreads();
+    scan::chunk_step<Tin, C, PER_K>(st, k, w, u, gcum, t0, Lc, hv, hq, H, HV, K, V, V, c0col, l2,
+                                     FINAL ? v_new : nullptr);
   }
   if (FINAL) {
     if (ht && cend == nch)
       for (int64_t e = tid; e < K * kTile; e += kThreads) {
         const int64_t d = e / kTile, col = c0col + e % kTile;
-        if (col < V) ht[((n * HV + hv) * K + d) * V + col] = hs[e];
+        if (col < V) ht[((n * HV + hv) * K + d) * V + col] = st.hs[d * scan::kHS + e % kTile];
       }
   } else {
     for (int64_t e = tid; e < K * kTile; e += kThreads) {
       const int64_t d = e / kTile, col = c0col + e % kTile;
-      if (col < ncol) X[((seg * HV + hv) * K + d) * (V + K) + col] = hs[e];
+      if (col < ncol) X[((seg * HV + hv) * K + d) * (V + K) + col] = st.hs[d * scan::kHS + e % kTile];
     }
   }
 }
@@ -211,7 +178,7 @@ int launch_seg_scan(const ChunkedArgs &a, const SplitArgs &sp) {
     constexpr bool PK = decltype(cfg)::PK;
     const int64_t K = a.d.K, V = a.d.V;
     const int64_t ncol = FINAL ? V : V + K;
-    const size_t smem = sizeof(float) * (K * kTile + 2 * C * K + C * kTile + K);
+    const size_t smem = sizeof(float) * scan::smem_floats(C, K);
     auto kern = seg_scan_kernel<Tin, C, PK, FINAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_error(e, "seg_scan_kernel");
