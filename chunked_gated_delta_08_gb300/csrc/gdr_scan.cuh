@@ -60,6 +60,58 @@ __device__ __forceinline__ void mma3(float (&d)[4], const uint32_t (&ah)[4], con
   sm100::mma_tf32(d, ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
 }
 
+// Kb rows (L2-normalized k times e^{G_L - G}) into kt and -w into ws, for the
+// chunk's rows, zero past Lc and past K.  Warp w takes rows w, w + 8, ...; the
+// loads of RB rows (KV values per lane and row) are all issued before any row
+// is reduced, so a warp waits on memory once per RB rows.
+template <typename Tin, int C, bool PER_K, int KV, int RB>
+__device__ __forceinline__ void load_rows(const Tiles &s, const Tin *__restrict__ k, const float *__restrict__ w,
+                                          const float *__restrict__ gcum, int64_t t0, int Lc, int64_t hv,
+                                          int64_t hq, int64_t H, int64_t HV, int64_t K, int l2) {
+  constexpr int kWarps = kScanThreads / 32;
+  constexpr int RPW = C / kWarps;  // rows per warp
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t Kp = kpad(K), WL = ws_ld(K), KL = kt_ld(K);
+  const int64_t gw = PER_K ? K : 1;
+#pragma unroll
+  for (int jb = 0; jb < RPW; jb += RB) {
+    float kv[RB][KV], gv[RB][KV], wv[RB][KV];
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      const int i = warp + kWarps * (jb + r);
+      const bool rok = jb + r < RPW && i < Lc;
+      const int64_t tok = t0 + i;
+#pragma unroll
+      for (int m = 0; m < KV; ++m) {
+        const int64_t d = lane + 32 * m;
+        const bool ok = rok && d < K;
+        kv[r][m] = ok ? to_f32(k[(tok * H + hq) * K + d]) : 0.f;
+        gv[r][m] = ok ? gcum[(tok * HV + hv) * gw + (PER_K ? d : 0)] : 0.f;
+        wv[r][m] = ok ? w[(tok * HV + hv) * K + d] : 0.f;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      if (jb + r >= RPW) break;
+      const int i = warp + kWarps * (jb + r);
+      const bool rok = i < Lc;
+      float ss = 0.f;
+#pragma unroll
+      for (int m = 0; m < KV; ++m) ss = fmaf(kv[r][m], kv[r][m], ss);
+      const float sc = l2 ? rsqrtf(warp_sum(ss) + kL2Eps) : 1.f;
+#pragma unroll
+      for (int m = 0; m < KV; ++m) {
+        const int64_t d = lane + 32 * m;
+        if (d < Kp) {
+          const bool ok = rok && d < K;
+          s.kt[i * KL + d] = ok ? kv[r][m] * sc * expf(s.gl[d] - gv[r][m]) : 0.f;
+          s.ws[i * WL + d] = ok ? -wv[r][m] : 0.f;
+        }
+      }
+    }
+  }
+}
+
 // One chunk.  Called by all 256 threads of the block; hs holds the entering
 // tile and holds the leaving one on return.  v_new_out (nullable) receives
 // v_new for rows < Lc and columns < ucols.  c0col is the tile's first column
@@ -80,16 +132,8 @@ __device__ __forceinline__ void chunk_step(const Tiles &s, const Tin *__restrict
   __syncthreads();
   // Kb and -w, zero past Lc and past K
   constexpr int kWarps = kScanThreads / 32;
-  for (int i = warp; i < C; i += kWarps) {
-    float *kr = s.kt + i * KL;
-    load_row_normed(k, t0 + i, H, hq, K, i < Lc, l2, kr, lane);
-    for (int64_t d = lane; d < Kp; d += 32) {
-      const bool ok = i < Lc && d < K;
-      const float gi = ok ? gcum[((t0 + i) * HV + hv) * gw + (PER_K ? d : 0)] : 0.f;
-      kr[d] = ok ? kr[d] * expf(s.gl[d] - gi) : 0.f;
-      s.ws[i * WL + d] = ok ? -w[((t0 + i) * HV + hv) * K + d] : 0.f;
-    }
-  }
+  if (K <= 128) load_rows<Tin, C, PER_K, 4, 4>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
+  else load_rows<Tin, C, PER_K, 8, 2>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
   __syncthreads();
 
   // ---- v_new = u - w h: C x 32, warp -> rows 16 (warp & 3) .., columns 16 (warp >> 2) ..
