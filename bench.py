@@ -413,6 +413,40 @@ def split_measurement(gdr, steps: int, warmup: int = 3):
                          "algorithmic_bytes_per_launch": byt}}
 
 
+def profile_pass(gdr):
+    """Every form once on a mid-size workload, for a per-kernel ncu capture:
+    fused, chunked and split forwards on one 32768-token GDN sequence with 32
+    heads; the recurrent decode step; the KDA backward on one 8192-token
+    sequence.  Inputs are freed between forms so a multi-pass capture saves and
+    restores little device memory."""
+    runs = []
+    w = wl.GDN_BF16_PROFILE
+    x = {k: (None if t is None else t.cuda()) for k, t in wl.make_inputs(w).items()}
+    for algo in ("fused", "chunked", "split"):
+        gdr.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], h0=x["h0"], use_qk_l2norm=True, algo=algo)
+        runs.append(f"{w.name}:{algo}")
+    del x
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    w = wl.GDN_BF16_DECODE
+    x = {k: (None if t is None else t.cuda()) for k, t in wl.make_inputs(w).items()}
+    gdr.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], h0=x["h0"], use_qk_l2norm=True, algo="recurrent",
+            final_state=x["h0"])
+    runs.append(f"{w.name}:recurrent")
+    del x
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    w = wl.KDA_BF16_PROFILE
+    x = {k: (None if t is None else t.cuda()) for k, t in wl.make_inputs(w).items()}
+    gdr.bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["do"], dht=x["dht"], h0=x["h0"],
+            cu_seqlens=x["cu_seqlens"], use_qk_l2norm=True)
+    runs.append(f"{w.name}:bwd")
+    torch.cuda.synchronize()
+    if gdr.device_status() != 0:
+        raise RuntimeError(f"device status after the profile pass: {gdr.last_error()}")
+    return {"runs": runs, "launches": gdr.launch_count()}
+
+
 def run_ours(args, w, world, rank, local):
     import chunked_gated_delta_08_gb300 as gdr
     pk = peaks()
@@ -535,13 +569,16 @@ def main():
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward measurement")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
     ap.add_argument("--no-split", action="store_true", help="skip the intra-sequence split measurement")
-    ap.add_argument("--mode", default="fwd", choices=["fwd", "bwd", "decode", "split"],
+    ap.add_argument("--mode", default="fwd", choices=["fwd", "bwd", "decode", "split", "profile"],
                     help="bwd / decode: run only that measurement and print it alone")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     w = wl.BY_NAME[args.workload]
     if args.mode != "fwd":  # one measurement alone (used for the profiles); one GPU
         import chunked_gated_delta_08_gb300 as gdr
+        if args.mode == "profile":
+            print(json.dumps({"mode": "profile", **profile_pass(gdr)}), flush=True)
+            return
         fn = {"bwd": bwd_measurement, "decode": decode_measurement, "split": split_measurement}[args.mode]
         res = fn(gdr, steps=args.steps, warmup=args.warmup)
         print(json.dumps({"mode": args.mode, **res}), flush=True)

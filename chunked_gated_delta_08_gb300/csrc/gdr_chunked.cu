@@ -5,8 +5,9 @@
 // debug-script layout: fwd_intra -> wy -> fwd_h -> o):
 //   chunk_index_kernel  cu_seqlens -> (sequence, chunk) map, int64
 //   prepare_kernel      per (chunk, value head): L2 norm of k, gate cumsum,
-//                       A = tril(beta K K^T * decay, -1), (I + A)^-1 applied by
-//                       forward substitution to give w and u
+//                       A = tril(beta K K^T * decay, -1), T = (I + A)^-1 by
+//                       blocks, w and u as products with T (tensor cores,
+//                       3 x TF32)
 //   fwd_h_kernel        per (sequence, value head, V-tile), sequential over
 //                       chunks: h (state entering the chunk), v_new = u - w h,
 //                       h <- exp(G_C) h + (K * exp(G_C - G))^T v_new, both
@@ -21,6 +22,7 @@
 
 #include "gdr_device.cuh"
 #include "gdr_internal.h"
+#include "gdr_prep.cuh"
 #include "gdr_scan.cuh"
 
 namespace gdr {
@@ -103,9 +105,32 @@ __global__ void chunk_index_kernel(const int64_t *__restrict__ cu, int64_t N, in
 }
 
 // --------------------------------------------------------------------------
-// prepare: grid (nt_max, HV)
-// smem: ks[C*K] | gam[C*K or C] | bet[C] | A[C*C]
+// prepare: grid (nt_max, HV).  Per (chunk, value head), on tensor cores in
+// 3 x TF32 wherever the work is a product:
+//   Gamma   within-chunk cumsum of g (written to gcum)
+//   A_ij    = beta_i sum_d k_id k_jd e^{G_id - G_jd}, i > j.  Scalar gate: the
+//             Gram matrix K K^T by tiles, then the decay per entry.  Per-key
+//             gate: the diagonal 16 x 16 blocks per entry; a block row a > 0
+//             against the rows before it as one product of
+//             k_i e^{G_i - G_r} and k_j e^{G_r - G_j}, r = 16 a, so both
+//             factors have non-positive exponents (the "safe gate" reading)
+//   T       = (I + A)^-1 by blocks (prep::solve_unit_lower)
+//   w, u    = T [diag(beta e^G) K | diag(beta) V], 64-column tiles
+// smem: ks[C][KL] | gam[C][Kp] or [C] | bet[C] | AT[C][C+1] | Tm[C][C+4] |
+//       Bt[C][72] | Xs[16][KL] | Ys[C][KL]   (KL = Kp + 4; Xs, Ys per-key, K <= 128)
 // --------------------------------------------------------------------------
+constexpr int kBtCols = 64;
+constexpr int kBtLd = kBtCols + 8;
+
+// The per-key gate's block-row products need two scaled copies of k (Xs, Ys);
+// past K = 128 they would not fit, and A is formed entry by entry instead.
+__host__ __device__ constexpr bool prep_factored(int64_t K) { return K <= 128; }
+
+__host__ __device__ constexpr int64_t prep_smem_floats(int C, int64_t K, bool per_k) {
+  return C * (scan::kpad(K) + 4) + (per_k ? C * scan::kpad(K) : C) + C + C * (C + 1) + C * (C + 4) + C * kBtLd +
+         (per_k && prep_factored(K) ? (16 + C) * (scan::kpad(K) + 4) : 0);
+}
+
 template <typename Tin, int C, bool PER_K>
 __global__ void __launch_bounds__(kThreads) prepare_kernel(
     const Tin *__restrict__ k, const Tin *__restrict__ v, const float *__restrict__ g,
@@ -113,11 +138,17 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(
     int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V, int l2, int beta_logits, float *__restrict__ gcum,
     float *__restrict__ w, float *__restrict__ u) {
   extern __shared__ float smem[];
+  const int64_t Kp = scan::kpad(K), KL = Kp + 4, GL = PER_K ? Kp : 1;
+  constexpr int LA = C + 1, LT = C + 4;
   float *ks = smem;
-  float *gam = ks + C * K;
-  float *bet = gam + (PER_K ? C * K : C);
-  float *A = bet + C;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float *gam = ks + C * KL;
+  float *bet = gam + (PER_K ? C * Kp : C);
+  float *AT = bet + C;
+  float *Tm = AT + C * LA;
+  float *Bt = Tm + C * LT;
+  float *Xs = Bt + C * kBtLd;
+  float *Ys = Xs + 16 * KL;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, gq = lane >> 2, tq = lane & 3;
   const int64_t chunk = blockIdx.x, hv = blockIdx.y;
   int64_t n, j;
   if (!chunk_coords(chunk_indices, chunk, T, C, &n, &j)) return;
@@ -125,70 +156,153 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(
   const int64_t t0 = sr.bos + j * C;
   const int Lc = (int)(sr.eos - t0 < (int64_t)C ? sr.eos - t0 : (int64_t)C);
   const int64_t hq = hv / (HV / H);
-
-  for (int i = warp; i < C; i += kWarps) load_row_normed(k, t0 + i, H, hq, K, i < Lc, l2, ks + i * K, lane);
-  // gate cumsum within the chunk: load every g in parallel, then scan in smem
   const int64_t gw = PER_K ? K : 1;
+
+  // ---- k rows (normalized), g, beta: four rows per warp in flight at a time
+  for (int i0 = warp; i0 < C; i0 += 4 * kWarps) {
+    float kv[4][8];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = i0 + kWarps * r;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int64_t d = lane + 32 * m;
+        kv[r][m] = (i < C && i < Lc && d < K) ? to_f32(k[((t0 + i) * H + hq) * K + d]) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = i0 + kWarps * r;
+      if (i >= C) break;
+      float ss = 0.f;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) ss = fmaf(kv[r][m], kv[r][m], ss);
+      const float sc = l2 ? rsqrtf(warp_sum(ss) + kL2Eps) : 1.f;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int64_t d = lane + 32 * m;
+        if (d < KL) ks[i * KL + d] = kv[r][m] * sc;  // zero past K and past Lc
+      }
+    }
+  }
   for (int64_t e = tid; e < C * gw; e += kThreads) {
     const int64_t i = e / gw, d = e % gw;
-    gam[e] = i < Lc ? g[((t0 + i) * HV + hv) * gw + d] : 0.f;
+    gam[i * GL + d] = i < Lc ? g[((t0 + i) * HV + hv) * gw + d] : 0.f;
   }
   for (int i = tid; i < C; i += kThreads) bet[i] = i < Lc ? load_beta(beta, (t0 + i) * HV + hv, beta_logits) : 0.f;
   __syncthreads();
-  for (int64_t d = tid; d < gw; d += kThreads) {
-    float s = 0.f;
+  for (int64_t d = tid; d < gw; d += kThreads) {  // inclusive cumsum down each column
+    float acc = 0.f;
     for (int i = 0; i < C; ++i) {
-      s += gam[i * gw + d];
-      gam[i * gw + d] = s;
+      acc += gam[i * GL + d];
+      gam[i * GL + d] = acc;
     }
   }
   __syncthreads();
   for (int64_t e = tid; e < Lc * gw; e += kThreads) {
     const int64_t i = e / gw, d = e % gw;
-    gcum[((t0 + i) * HV + hv) * gw + d] = gam[e];
+    gcum[((t0 + i) * HV + hv) * gw + d] = gam[i * GL + d];
   }
 
-  // A_ij = beta_i sum_d k_id k_jd exp(G_id - G_jd), i > j
-  for (int p = warp; p < C * C; p += kWarps) {
-    const int i = p / C, jj = p % C;
-    if (jj >= i || i >= Lc) {
-      if (lane == 0) A[p] = 0.f;
-      continue;
+  // ---- A (strictly lower) into AT
+  const int nk = (int)(Kp / 8);
+  if (!PER_K) {
+    // lower-triangle tiles of K K^T: row tile a (16 rows) x column tiles 0 .. 2a+1 (8 cols)
+    for (int tix = warp; tix < (C / 16) * (C / 16 + 1); tix += kWarps) {
+      int a = 0, rem = tix;
+      while (rem >= 2 * a + 2) {
+        rem -= 2 * a + 2;
+        ++a;
+      }
+      const int m0 = 16 * a, n0 = 8 * rem;
+      float d[4];
+      prep::tile<true>(d, ks, KL, ks, KL, m0, n0, nk);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = m0 + gq + 8 * (e >> 1), jj = n0 + 2 * tq + (e & 1);
+        AT[i * LA + jj] = (jj < i && i < Lc) ? bet[i] * expf(gam[i] - gam[jj]) * d[e] : 0.f;
+      }
     }
-    float s = 0.f;
-    for (int64_t d = lane; d < K; d += 32) {
-      float t = ks[i * K + d] * ks[jj * K + d];
-      if (PER_K) t *= expf(gam[i * K + d] - gam[jj * K + d]);
-      s += t;
+  } else {
+    // diagonal 16 x 16 blocks entry by entry (one warp per entry, lanes over d);
+    // every entry so when K is too large for the block-row products
+    const bool factored = prep_factored(K);
+    const int per_row = factored ? 16 : C;
+    for (int p = warp; p < C * per_row; p += kWarps) {
+      const int i = p / per_row, jj = (factored ? 16 * (i / 16) : 0) + p % per_row;
+      if (jj >= i || i >= Lc) {
+        if (lane == 0) AT[i * LA + jj] = 0.f;
+        continue;
+      }
+      float acc = 0.f;
+      for (int64_t d = lane; d < K; d += 32)
+        acc = fmaf(ks[i * KL + d] * ks[jj * KL + d], expf(gam[i * GL + d] - gam[jj * GL + d]), acc);
+      acc = warp_sum(acc);
+      if (lane == 0) AT[i * LA + jj] = bet[i] * acc;
     }
-    s = warp_sum(s);
-    if (lane == 0) A[p] = bet[i] * s * (PER_K ? 1.f : expf(gam[i] - gam[jj]));
+    // block row a against rows 0 .. 16a-1 through the reference row r = 16a
+    for (int a = 1; factored && a < C / 16; ++a) {
+      const int r = 16 * a;
+      __syncthreads();
+      for (int64_t e = tid; e < (16 + r) * Kp; e += kThreads) {
+        const int row = (int)(e / Kp);
+        const int64_t d = e % Kp;
+        if (row < 16) {
+          const int i = r + row;
+          Xs[row * KL + d] = d < K ? ks[i * KL + d] * expf(gam[i * GL + d] - gam[r * GL + d]) : 0.f;
+        } else {
+          const int jr = row - 16;
+          Ys[jr * KL + d] = d < K ? ks[jr * KL + d] * expf(gam[r * GL + d] - gam[jr * GL + d]) : 0.f;
+        }
+      }
+      __syncthreads();
+      for (int nt = warp; nt < r / 8; nt += kWarps) {
+        float d[4];
+        prep::tile<true>(d, Xs, KL, Ys, KL, 0, 8 * nt, nk);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = r + gq + 8 * (e >> 1), jj = 8 * nt + 2 * tq + (e & 1);
+          AT[i * LA + jj] = i < Lc ? bet[i] * d[e] : 0.f;
+        }
+      }
+    }
   }
   __syncthreads();
 
-  // (I + A) x = rhs by forward substitution, one column per thread:
-  // columns [0, K) give w (rhs beta_i exp(G_i) k_i), columns [K, K+V) give u (rhs beta_i v_i)
-  for (int64_t col = tid; col < K + V; col += kThreads) {
-    float x[C];
-    const bool is_w = col < K;
-#pragma unroll
-    for (int i = 0; i < C; ++i) {
-      float rhs;
-      if (is_w) {
-        rhs = bet[i] * ks[i * K + col] * expf(PER_K ? gam[i * K + col] : gam[i]);
-      } else {
-        rhs = i < Lc ? bet[i] * to_f32(v[((t0 + i) * HV + hv) * V + (col - K)]) : 0.f;
+  // ---- T = (I + A)^-1, then dense into Tm (row-major, diagonal 1)
+  prep::solve_unit_lower<C>(AT, LA, Bt);
+  for (int e = tid; e < C * C; e += kThreads) {
+    const int i = e / C, jj = e % C;
+    Tm[i * LT + jj] = prep::t_at(AT, LA, i, jj);
+  }
+
+  // ---- [w | u] = T [diag(beta e^G) K | diag(beta) V], 64 columns at a time
+  const int64_t ncol = K + V;
+  for (int64_t c0 = 0; c0 < ncol; c0 += kBtCols) {
+    __syncthreads();  // Tm complete; the previous tile's reads of Bt done
+    for (int e = tid; e < C * kBtCols; e += kThreads) {
+      const int jj = e / kBtCols, cc = e % kBtCols;
+      const int64_t col = c0 + cc;
+      float x = 0.f;
+      if (jj < Lc && col < ncol) {
+        if (col < K) x = bet[jj] * expf(PER_K ? gam[jj * GL + col] : gam[jj]) * ks[jj * KL + col];
+        else x = bet[jj] * to_f32(v[((t0 + jj) * HV + hv) * V + (col - K)]);
       }
-      float acc = rhs;
-#pragma unroll
-      for (int jj = 0; jj < i; ++jj) acc = fmaf(-A[i * C + jj], x[jj], acc);
-      x[i] = acc;
+      Bt[jj * kBtLd + cc] = x;
     }
+    __syncthreads();
+    for (int tix = warp; tix < (C / 16) * (kBtCols / 8); tix += kWarps) {
+      const int m0 = 16 * (tix % (C / 16)), n0 = 8 * (tix / (C / 16));
+      float d[4];
+      prep::tile<false>(d, Tm, LT, Bt, kBtLd, m0, n0, C / 8);
 #pragma unroll
-    for (int i = 0; i < C; ++i) {
-      if (i < Lc) {
-        if (is_w) w[((t0 + i) * HV + hv) * K + col] = x[i];
-        else u[((t0 + i) * HV + hv) * V + (col - K)] = x[i];
+      for (int e = 0; e < 4; ++e) {
+        const int i = m0 + gq + 8 * (e >> 1);
+        const int64_t col = c0 + n0 + 2 * tq + (e & 1);
+        if (i < Lc && col < ncol) {
+          if (col < K) w[((t0 + i) * HV + hv) * K + col] = d[e];
+          else u[((t0 + i) * HV + hv) * V + (col - K)] = d[e];
+        }
       }
     }
   }
@@ -362,7 +476,7 @@ static int prepare_t(const ChunkedArgs &a) {
   return dispatch_cfg(a.C, a.d.gate == GDR_GATE_PER_K, [&](auto cfg) {
     constexpr int CC = decltype(cfg)::C;
     constexpr bool PK = decltype(cfg)::PK;
-    const size_t smem = sizeof(float) * (CC * K + (PK ? CC * K : CC) + CC + CC * CC);
+    const size_t smem = sizeof(float) * prep_smem_floats(CC, K, PK);
     auto kern = prepare_kernel<Tin, CC, PK>;
     dim3 grid((unsigned)a.nt_max, (unsigned)a.d.HV);
     int rc = launch_checked(kern, grid, smem, a.stream, "prepare_kernel");

@@ -1,0 +1,155 @@
+// gdr_prep.cuh -- tensor-core building blocks of the chunked form's
+// per-chunk preparation: 16 x 8 warp tiles of shared-memory products in
+// 3 x TF32 (close to fp32), and T = (I + A)^-1 of a unit lower-triangular
+// C x C matrix by blocks (the UT transform behind the WY representation of
+// the coverage guide, section 二).
+//
+// Fragment layout of mma.sync m16n8k8 (g = lane / 4, t = lane % 4): A (16x8)
+// (g, t) (g+8, t) (g, t+4) (g+8, t+4); B (8x8, K x N) (t, g) (t+4, g);
+// D (16x8) (g, 2t) (g, 2t+1) (g+8, 2t) (g+8, 2t+1).
+#pragma once
+
+#include "gdr_scan.cuh"
+
+namespace gdr {
+namespace prep {
+
+// d (16 x 8 tile, rows m0.., cols n0..) = sum over k < 8 nk of A(m, k) B(k, n):
+// A(m, k) = a[m lda + k];  B(k, n) = TB ? b[n ldb + k] : b[k ldb + n].
+// Conflict-free when lda (and ldb for TB) is 4 mod 32, or ldb 8 mod 32 otherwise.
+template <bool TB>
+__device__ __forceinline__ void tile(float (&d)[4], const float *a, int64_t lda, const float *b, int64_t ldb,
+                                     int m0, int n0, int nk) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) d[e] = 0.f;
+  for (int ks = 0; ks < nk; ++ks) {
+    const int k0 = 8 * ks;
+    uint32_t ah[4], al[4], bh[2], bl[2];
+    const float *ar = a + (int64_t)(m0 + g) * lda + k0 + t;
+    scan::split3(ar[0], ah[0], al[0]);
+    scan::split3(ar[8 * lda], ah[1], al[1]);
+    scan::split3(ar[4], ah[2], al[2]);
+    scan::split3(ar[8 * lda + 4], ah[3], al[3]);
+    if (TB) {
+      const float *br = b + (int64_t)(n0 + g) * ldb + k0 + t;
+      scan::split3(br[0], bh[0], bl[0]);
+      scan::split3(br[4], bh[1], bl[1]);
+    } else {
+      const float *br = b + (int64_t)(k0 + t) * ldb + n0 + g;
+      scan::split3(br[0], bh[0], bl[0]);
+      scan::split3(br[4 * ldb], bh[1], bl[1]);
+    }
+    scan::mma3(d, ah, al, bh, bl);
+  }
+}
+
+// The same with A and B read through functors fa(m, k), fb(k, n) (tile-local
+// indices), for the triangular operands of the solve.
+template <typename FA, typename FB>
+__device__ __forceinline__ void tile_f(float (&d)[4], int nk, FA fa, FB fb) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) d[e] = 0.f;
+  for (int ks = 0; ks < nk; ++ks) {
+    const int k0 = 8 * ks;
+    uint32_t ah[4], al[4], bh[2], bl[2];
+    scan::split3(fa(g, k0 + t), ah[0], al[0]);
+    scan::split3(fa(g + 8, k0 + t), ah[1], al[1]);
+    scan::split3(fa(g, k0 + t + 4), ah[2], al[2]);
+    scan::split3(fa(g + 8, k0 + t + 4), ah[3], al[3]);
+    scan::split3(fb(k0 + t, g), bh[0], bl[0]);
+    scan::split3(fb(k0 + t + 4, g), bh[1], bl[1]);
+    scan::mma3(d, ah, al, bh, bl);
+  }
+}
+
+// T[r][s] from the packed array: A strictly below the diagonal of AT (row
+// stride lda), T's strict lower part stored transposed above it.
+__device__ __forceinline__ float t_at(const float *AT, int lda, int r, int s) {
+  return r > s ? AT[s * lda + r] : (r == s ? 1.f : 0.f);
+}
+
+// T = (I + A)^-1 for the C x C unit lower-triangular I + A held strictly below
+// the diagonal of AT; T's strict lower part is written transposed strictly
+// above the diagonal (T_ij at AT[j][i]).  Blocks: 16 x 16 diagonal inverses by
+// forward substitution, then [[T1, 0], [T21, T2]] with T21 = -T2 A21 T1 for
+// 16 -> 32 and (C = 64) 32 -> 64.  All 256 threads; X is scratch of 1536
+// floats.
+template <int C>
+__device__ void solve_unit_lower(float *AT, int lda, float *X) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  if (warp < C / 16 && lane < 16) {
+    const int base = 16 * warp, c = lane;
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float a0 = (i == c) ? 1.f : 0.f, a1 = 0.f;
+#pragma unroll
+      for (int l = 0; l < i; l += 2) {
+        a0 = fmaf(-AT[(base + i) * lda + base + l], x[l], a0);
+        if (l + 1 < i) a1 = fmaf(-AT[(base + i) * lda + base + l + 1], x[l + 1], a1);
+      }
+      x[i] = (i < c) ? 0.f : a0 + a1;
+    }
+#pragma unroll
+    for (int i = 1; i < 16; ++i)
+      if (i > c) AT[(base + c) * lda + base + i] = x[i];
+  }
+  __syncthreads();
+  // 16 -> 32: pair p (blocks 2p+1, 2p), n-tile nt; warp = 2p + nt
+  if (warp < C / 16) {
+    const int p = warp >> 1, nt = warp & 1, r0 = 32 * p + 16, c0 = 32 * p;
+    float *Z = X + p * 256;
+    float d[4];
+    tile_f(d, 2, [&](int r, int k) { return AT[(r0 + r) * lda + c0 + k]; },
+           [&](int k, int n) { return t_at(AT, lda, c0 + k, c0 + 8 * nt + n); });
+    Z[g * 16 + 8 * nt + 2 * t] = d[0];
+    Z[g * 16 + 8 * nt + 2 * t + 1] = d[1];
+    Z[(g + 8) * 16 + 8 * nt + 2 * t] = d[2];
+    Z[(g + 8) * 16 + 8 * nt + 2 * t + 1] = d[3];
+  }
+  __syncthreads();
+  if (warp < C / 16) {
+    const int p = warp >> 1, nt = warp & 1, r0 = 32 * p + 16, c0 = 32 * p;
+    const float *Z = X + p * 256;
+    float d[4];
+    tile_f(d, 2, [&](int r, int k) { return t_at(AT, lda, r0 + r, r0 + k); },
+           [&](int k, int n) { return Z[k * 16 + 8 * nt + n]; });
+    const int cc = c0 + 8 * nt + 2 * t;
+    AT[cc * lda + r0 + g] = -d[0];
+    AT[(cc + 1) * lda + r0 + g] = -d[1];
+    AT[cc * lda + r0 + g + 8] = -d[2];
+    AT[(cc + 1) * lda + r0 + g + 8] = -d[3];
+  }
+  __syncthreads();
+  if (C == 64) {
+    // 32 -> 64: Y = A[32:64, 0:32] T[0:32, 0:32]; T[32:64, 0:32] = -T[32:64, 32:64] Y (one 16 x 8 tile per warp)
+    const int mt = warp >> 2, nt = warp & 3;
+    float *Y = X + 512;
+    {
+      float d[4];
+      tile_f(d, 4, [&](int r, int k) { return AT[(32 + 16 * mt + r) * lda + k]; },
+             [&](int k, int n) { return t_at(AT, lda, k, 8 * nt + n); });
+      Y[(16 * mt + g) * 32 + 8 * nt + 2 * t] = d[0];
+      Y[(16 * mt + g) * 32 + 8 * nt + 2 * t + 1] = d[1];
+      Y[(16 * mt + g + 8) * 32 + 8 * nt + 2 * t] = d[2];
+      Y[(16 * mt + g + 8) * 32 + 8 * nt + 2 * t + 1] = d[3];
+    }
+    __syncthreads();
+    {
+      float d[4];
+      tile_f(d, 4, [&](int r, int k) { return t_at(AT, lda, 32 + 16 * mt + r, 32 + k); },
+             [&](int k, int n) { return Y[k * 32 + 8 * nt + n]; });
+      const int cc = 8 * nt + 2 * t, rr = 32 + 16 * mt + g;
+      AT[cc * lda + rr] = -d[0];
+      AT[(cc + 1) * lda + rr] = -d[1];
+      AT[cc * lda + rr + 8] = -d[2];
+      AT[(cc + 1) * lda + rr + 8] = -d[3];
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace prep
+}  // namespace gdr

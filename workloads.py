@@ -88,7 +88,13 @@ GDN_BF16_DECODE = Workload("gdn_bf16_decode_N256_T1_H32_K128", torch.bfloat16, B
 GDN_FP32_LONG_FEW = Workload("gdn_fp32_B1_T32768_H4_K128", torch.float32, B=1, T=32768, H=4, HV=4, K=128, V=128,
                              use_qk_l2norm=True, h0_scale=0.1)
 
-BY_NAME = {w.name: w for w in WORKLOADS + [GDN_BF16_PROFILE, GDN_BF16_DECODE, GDN_FP32_LONG_FEW]}
+# A one-sequence cut of the KDA workload (8192 tokens) for per-kernel ncu
+# counters of the backward without the full workload's scratch.
+KDA_BF16_PROFILE = Workload("kda_bf16_T8192_HV32_V256", torch.bfloat16, B=1, T=8192, H=16, HV=32, K=128, V=256,
+                            lengths=(8192,), use_qk_l2norm=True, gate_per_k=True, gate_div=4.0, h0_scale=0.1,
+                            grads=True)
+
+BY_NAME = {w.name: w for w in WORKLOADS + [GDN_BF16_PROFILE, GDN_BF16_DECODE, GDN_FP32_LONG_FEW, KDA_BF16_PROFILE]}
 
 
 def make_inputs(w: Workload, device="cpu", seed: int | None = None) -> dict:
