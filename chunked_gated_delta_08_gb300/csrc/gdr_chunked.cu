@@ -13,7 +13,8 @@
 //                       h <- exp(G_C) h + (K * exp(G_C - G))^T v_new, both
 //                       products on tensor cores in 3 x TF32 (gdr_scan.cuh)
 //   fwd_o_kernel        per (chunk, value head): o = (q * exp G) h + P v_new
-//                       with P = tril(q k^T * decay) (diagonal included)
+//                       with P = tril(q k^T * decay) (diagonal included),
+//                       on tensor cores (3 x TF32)
 //
 // Decay factors are always formed as exp(G_i - G_j) with i >= j, so every
 // exponent is <= 0 and nothing overflows, whatever the gate values.
@@ -122,13 +123,9 @@ __global__ void chunk_index_kernel(const int64_t *__restrict__ cu, int64_t N, in
 constexpr int kBtCols = 64;
 constexpr int kBtLd = kBtCols + 8;
 
-// The per-key gate's block-row products need two scaled copies of k (Xs, Ys);
-// past K = 128 they would not fit, and A is formed entry by entry instead.
-__host__ __device__ constexpr bool prep_factored(int64_t K) { return K <= 128; }
-
 __host__ __device__ constexpr int64_t prep_smem_floats(int C, int64_t K, bool per_k) {
   return C * (scan::kpad(K) + 4) + (per_k ? C * scan::kpad(K) : C) + C + C * (C + 1) + C * (C + 4) + C * kBtLd +
-         (per_k && prep_factored(K) ? (16 + C) * (scan::kpad(K) + 4) : 0);
+         prep::gram_scratch_floats(C, K, per_k);
 }
 
 template <typename Tin, int C, bool PER_K>
@@ -157,6 +154,8 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(
   const int Lc = (int)(sr.eos - t0 < (int64_t)C ? sr.eos - t0 : (int64_t)C);
   const int64_t hq = hv / (HV / H);
   const int64_t gw = PER_K ? K : 1;
+  const int nk = (int)(Kp / 8);
+  (void)nk;
 
   // ---- k rows (normalized), g, beta: four rows per warp in flight at a time
   for (int i0 = warp; i0 < C; i0 += 4 * kWarps) {
@@ -205,69 +204,7 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(
   }
 
   // ---- A (strictly lower) into AT
-  const int nk = (int)(Kp / 8);
-  if (!PER_K) {
-    // lower-triangle tiles of K K^T: row tile a (16 rows) x column tiles 0 .. 2a+1 (8 cols)
-    for (int tix = warp; tix < (C / 16) * (C / 16 + 1); tix += kWarps) {
-      int a = 0, rem = tix;
-      while (rem >= 2 * a + 2) {
-        rem -= 2 * a + 2;
-        ++a;
-      }
-      const int m0 = 16 * a, n0 = 8 * rem;
-      float d[4];
-      prep::tile<true>(d, ks, KL, ks, KL, m0, n0, nk);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = m0 + gq + 8 * (e >> 1), jj = n0 + 2 * tq + (e & 1);
-        AT[i * LA + jj] = (jj < i && i < Lc) ? bet[i] * expf(gam[i] - gam[jj]) * d[e] : 0.f;
-      }
-    }
-  } else {
-    // diagonal 16 x 16 blocks entry by entry (one warp per entry, lanes over d);
-    // every entry so when K is too large for the block-row products
-    const bool factored = prep_factored(K);
-    const int per_row = factored ? 16 : C;
-    for (int p = warp; p < C * per_row; p += kWarps) {
-      const int i = p / per_row, jj = (factored ? 16 * (i / 16) : 0) + p % per_row;
-      if (jj >= i || i >= Lc) {
-        if (lane == 0) AT[i * LA + jj] = 0.f;
-        continue;
-      }
-      float acc = 0.f;
-      for (int64_t d = lane; d < K; d += 32)
-        acc = fmaf(ks[i * KL + d] * ks[jj * KL + d], expf(gam[i * GL + d] - gam[jj * GL + d]), acc);
-      acc = warp_sum(acc);
-      if (lane == 0) AT[i * LA + jj] = bet[i] * acc;
-    }
-    // block row a against rows 0 .. 16a-1 through the reference row r = 16a
-    for (int a = 1; factored && a < C / 16; ++a) {
-      const int r = 16 * a;
-      __syncthreads();
-      for (int64_t e = tid; e < (16 + r) * Kp; e += kThreads) {
-        const int row = (int)(e / Kp);
-        const int64_t d = e % Kp;
-        if (row < 16) {
-          const int i = r + row;
-          Xs[row * KL + d] = d < K ? ks[i * KL + d] * expf(gam[i * GL + d] - gam[r * GL + d]) : 0.f;
-        } else {
-          const int jr = row - 16;
-          Ys[jr * KL + d] = d < K ? ks[jr * KL + d] * expf(gam[r * GL + d] - gam[jr * GL + d]) : 0.f;
-        }
-      }
-      __syncthreads();
-      for (int nt = warp; nt < r / 8; nt += kWarps) {
-        float d[4];
-        prep::tile<true>(d, Xs, KL, Ys, KL, 0, 8 * nt, nk);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = r + gq + 8 * (e >> 1), jj = 8 * nt + 2 * tq + (e & 1);
-          AT[i * LA + jj] = i < Lc ? bet[i] * d[e] : 0.f;
-        }
-      }
-    }
-  }
-  __syncthreads();
+  prep::decayed_gram<C, PER_K, true>(ks, ks, KL, gam, GL, K, Lc, bet, AT, LA, Xs, Ys);
 
   // ---- T = (I + A)^-1, then dense into Tm (row-major, diagonal 1)
   prep::solve_unit_lower<C>(AT, LA, Bt);
@@ -353,9 +290,25 @@ __global__ void __launch_bounds__(kThreads) fwd_h_kernel(
 }
 
 // --------------------------------------------------------------------------
-// fwd_o: grid (nt_max, HV).  V is walked in tiles of C columns.
-// smem: qs[C*K] | ks[C*K] (reused for the h tile [K*C]) | gam[C*K or C] | P[C*C] | vn[C*C]
+// fwd_o: grid (nt_max, HV).  P = tril(q k^T * decay) (diagonal included) by
+// prep::decayed_gram, then per 32-column V tile o = (q * e^G) h + P v_new as
+// two tensor-core products (3 x TF32).
+// smem: qs[C][KL] | ks[C][KL] (then the h tile [Kp][40]) | gam | P[C][C+4] |
+//       vn[C][40] | Xs, Ys (per-key gate, K <= 128)
 // --------------------------------------------------------------------------
+constexpr int kOCols = 32;
+constexpr int kOLd = kOCols + 8;
+
+// the ks region also holds the h tile later
+__host__ __device__ constexpr int64_t fwd_o_ks_floats(int C, int64_t K) {
+  return C * (scan::kpad(K) + 4) > scan::kpad(K) * kOLd ? C * (scan::kpad(K) + 4) : scan::kpad(K) * kOLd;
+}
+
+__host__ __device__ constexpr int64_t fwd_o_smem_floats(int C, int64_t K, bool per_k) {
+  return C * (scan::kpad(K) + 4) + fwd_o_ks_floats(C, K) + (per_k ? C * scan::kpad(K) : C) + C * (C + 4) +
+         C * kOLd + prep::gram_scratch_floats(C, K, per_k);
+}
+
 template <typename Tin, int C, bool PER_K>
 __global__ void __launch_bounds__(kThreads) fwd_o_kernel(
     const Tin *__restrict__ q, const Tin *__restrict__ k, const float *__restrict__ v_new,
@@ -363,13 +316,17 @@ __global__ void __launch_bounds__(kThreads) fwd_o_kernel(
     const int64_t *__restrict__ chunk_indices, int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V,
     int l2, Tin *__restrict__ o) {
   extern __shared__ float smem[];
+  const int64_t Kp = scan::kpad(K), KL = Kp + 4, GL = PER_K ? Kp : 1;
+  constexpr int LP = C + 4;
   float *qs = smem;
-  float *ks = qs + C * K;
+  float *ks = qs + C * KL;
   float *hs = ks;
-  float *gam = ks + C * K;
-  float *P = gam + (PER_K ? C * K : C);
-  float *vn = P + C * C;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float *gam = ks + fwd_o_ks_floats(C, K);
+  float *P = gam + (PER_K ? C * Kp : C);
+  float *vn = P + C * LP;
+  float *Xs = vn + C * kOLd;
+  float *Ys = Xs + 16 * KL;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, gq = lane >> 2, tq = lane & 3;
   const int64_t chunk = blockIdx.x, hv = blockIdx.y;
   int64_t n, j;
   if (!chunk_coords(chunk_indices, chunk, T, C, &n, &j)) return;
@@ -377,60 +334,80 @@ __global__ void __launch_bounds__(kThreads) fwd_o_kernel(
   const int64_t t0 = sr.bos + j * C;
   const int Lc = (int)(sr.eos - t0 < (int64_t)C ? sr.eos - t0 : (int64_t)C);
   const int64_t hq = hv / (HV / H);
+  const int64_t gw = PER_K ? K : 1;
 
-  for (int i = warp; i < C; i += kWarps) {
-    load_row_normed(q, t0 + i, H, hq, K, i < Lc, l2, qs + i * K, lane);
-    load_row_normed(k, t0 + i, H, hq, K, i < Lc, l2, ks + i * K, lane);
-  }
-  if (PER_K) {
-    for (int64_t e = tid; e < C * K; e += kThreads) {
-      const int64_t i = e / K, d = e % K;
-      gam[e] = i < Lc ? gcum[((t0 + i) * HV + hv) * K + d] : 0.f;
-    }
-  } else {
-    for (int i = tid; i < C; i += kThreads) gam[i] = i < Lc ? gcum[(t0 + i) * HV + hv] : 0.f;
-  }
-  __syncthreads();
-  // P_ri = sum_d q_rd k_id exp(G_rd - G_id), i <= r
-  for (int p = warp; p < C * C; p += kWarps) {
-    const int r = p / C, i = p % C;
-    if (i > r || r >= Lc) {
-      if (lane == 0) P[p] = 0.f;
-      continue;
-    }
-    float s = 0.f;
-    for (int64_t d = lane; d < K; d += 32) {
-      float t = qs[r * K + d] * ks[i * K + d];
-      if (PER_K) t *= expf(gam[r * K + d] - gam[i * K + d]);
-      s += t;
-    }
-    s = warp_sum(s);
-    if (lane == 0) P[p] = s * (PER_K ? 1.f : expf(gam[r] - gam[i]));
-  }
-  __syncthreads();
-  for (int64_t e = tid; e < C * K; e += kThreads) qs[e] *= expf(PER_K ? gam[e] : gam[e / K]);
-  __syncthreads();
-
-  for (int64_t v0 = 0; v0 < V; v0 += C) {
-    for (int64_t e = tid; e < K * C; e += kThreads) {
-      const int64_t d = e / C, vv = e % C;
-      hs[e] = v0 + vv < V ? h[((chunk * HV + hv) * K + d) * V + v0 + vv] : 0.f;
-    }
-    for (int64_t e = tid; e < C * C; e += kThreads) {
-      const int64_t i = e / C, vv = e % C;
-      vn[e] = (i < Lc && v0 + vv < V) ? v_new[((t0 + i) * HV + hv) * V + v0 + vv] : 0.f;
-    }
-    __syncthreads();
-    for (int64_t e = tid; e < C * C; e += kThreads) {
-      const int r = (int)(e / C), vv = (int)(e % C);
-      if (r < Lc && v0 + vv < V) {
-        float acc = 0.f;
-        for (int64_t d = 0; d < K; ++d) acc = fmaf(qs[r * K + d], hs[d * C + vv], acc);
-        for (int i = 0; i <= r; ++i) acc = fmaf(P[r * C + i], vn[i * C + vv], acc);
-        o[((t0 + r) * HV + hv) * V + v0 + vv] = from_f32<Tin>(acc);
+  // q and k rows (normalized), four rows per warp in flight at a time
+  for (int i0 = warp; i0 < C; i0 += 4 * kWarps) {
+    float qv[4][8], kv[4][8];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = i0 + kWarps * r;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int64_t d = lane + 32 * m;
+        const bool ok = i < C && i < Lc && d < K;
+        qv[r][m] = ok ? to_f32(q[((t0 + i) * H + hq) * K + d]) : 0.f;
+        kv[r][m] = ok ? to_f32(k[((t0 + i) * H + hq) * K + d]) : 0.f;
       }
     }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = i0 + kWarps * r;
+      if (i >= C) break;
+      float sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        sq = fmaf(qv[r][m], qv[r][m], sq);
+        sk = fmaf(kv[r][m], kv[r][m], sk);
+      }
+      const float cq = l2 ? rsqrtf(warp_sum(sq) + kL2Eps) : 1.f, ck = l2 ? rsqrtf(warp_sum(sk) + kL2Eps) : 1.f;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int64_t d = lane + 32 * m;
+        if (d < KL) {
+          qs[i * KL + d] = qv[r][m] * cq;
+          ks[i * KL + d] = kv[r][m] * ck;
+        }
+      }
+    }
+  }
+  for (int64_t e = tid; e < C * gw; e += kThreads) {
+    const int64_t i = e / gw, d = e % gw;
+    gam[i * GL + d] = i < Lc ? gcum[((t0 + i) * HV + hv) * gw + d] : 0.f;
+  }
+  for (int e = tid; e < C * LP; e += kThreads) P[e] = 0.f;  // the product reads P's upper part too
+  __syncthreads();
+  prep::decayed_gram<C, PER_K, false>(qs, ks, KL, gam, GL, K, Lc, nullptr, P, LP, Xs, Ys);
+  // q * e^G in place
+  for (int64_t e = tid; e < C * Kp; e += kThreads) {
+    const int i = (int)(e / Kp);
+    const int64_t d = e % Kp;
+    if (d < K) qs[i * KL + d] *= expf(PER_K ? gam[i * GL + d] : gam[i]);
+  }
+
+  for (int64_t v0 = 0; v0 < V; v0 += kOCols) {
+    __syncthreads();  // q * e^G done; the previous tile's reads of hs and vn done
+    for (int64_t e = tid; e < Kp * kOCols; e += kThreads) {
+      const int64_t d = e / kOCols, vv = e % kOCols;
+      hs[d * kOLd + vv] = (d < K && v0 + vv < V) ? h[((chunk * HV + hv) * K + d) * V + v0 + vv] : 0.f;
+    }
+    for (int e = tid; e < C * kOCols; e += kThreads) {
+      const int i = e / kOCols, vv = e % kOCols;
+      vn[i * kOLd + vv] = (i < Lc && v0 + vv < V) ? v_new[((t0 + i) * HV + hv) * V + v0 + vv] : 0.f;
+    }
     __syncthreads();
+    for (int tix = warp; tix < (C / 16) * (kOCols / 8); tix += kWarps) {
+      const int m0 = 16 * (tix % (C / 16)), n0 = 8 * (tix / (C / 16));
+      float d1[4], d2[4];
+      prep::tile<false>(d1, qs, KL, hs, kOLd, m0, n0, (int)(Kp / 8));
+      prep::tile<false>(d2, P, LP, vn, kOLd, m0, n0, C / 8);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = m0 + gq + 8 * (e >> 1);
+        const int64_t col = v0 + n0 + 2 * tq + (e & 1);
+        if (i < Lc && col < V) o[((t0 + i) * HV + hv) * V + col] = from_f32<Tin>(d1[e] + d2[e]);
+      }
+    }
   }
 }
 
@@ -515,7 +492,7 @@ static int fwd_o_t(const ChunkedArgs &a) {
   return dispatch_cfg(a.C, a.d.gate == GDR_GATE_PER_K, [&](auto cfg) {
     constexpr int CC = decltype(cfg)::C;
     constexpr bool PK = decltype(cfg)::PK;
-    const size_t smem = sizeof(float) * (2 * CC * K + (PK ? CC * K : CC) + 2 * CC * CC);
+    const size_t smem = sizeof(float) * fwd_o_smem_floats(CC, K, PK);
     auto kern = fwd_o_kernel<Tin, CC, PK>;
     dim3 grid((unsigned)a.nt_max, (unsigned)a.d.HV);
     int rc = launch_checked(kern, grid, smem, a.stream, "fwd_o_kernel");

@@ -151,5 +151,94 @@ __device__ void solve_unit_lower(float *AT, int lda, float *X) {
   }
 }
 
+// The per-key gate's block-row products need two scaled copies of the rows
+// (Xs, Ys); past K = 128 they would not fit, and every entry is formed
+// directly instead.
+__host__ __device__ constexpr bool gram_factored(int64_t K) { return K <= 128; }
+
+// Floats of scratch (Xs, Ys) decayed_gram needs for K (row stride kpad(K)+4).
+__host__ __device__ constexpr int64_t gram_scratch_floats(int C, int64_t K, bool per_k) {
+  return per_k && gram_factored(K) ? (16 + C) * (scan::kpad(K) + 4) : 0;
+}
+
+// out[i][j] = s_i sum_d X_id Y_jd e^{G_id - G_jd} for j < i (STRICT) or
+// j <= i, i < Lc; 0 elsewhere (out row stride lo).  X, Y rows have stride xl
+// (= kpad(K) + 4, zero past K); gam is G per row (scalar gate, gl = 1) or per
+// row and channel (stride gl); s (nullable) is a row scale.  Scalar gate: the
+// Gram tiles, then e^{G_i - G_j} per entry.  Per-key gate: diagonal 16 x 16
+// blocks entry by entry; block row a > 0 against rows 0 .. 16a-1 as one
+// product of X_i e^{G_i - G_r} and Y_j e^{G_r - G_j}, r = 16 a, so no factor
+// has a positive exponent for non-positive gates.  All 256 threads; ends
+// with a barrier.
+template <int C, bool PER_K, bool STRICT>
+__device__ void decayed_gram(const float *X, const float *Y, int64_t xl, const float *gam, int64_t gl, int64_t K,
+                             int Lc, const float *s, float *out, int lo, float *Xs, float *Ys) {
+  constexpr int kWarps = 8;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, gq = lane >> 2, tq = lane & 3;
+  const int64_t Kp = scan::kpad(K);
+  const int nk = (int)(Kp / 8);
+  auto below = [](int i, int j) { return STRICT ? j < i : j <= i; };
+  if (!PER_K) {
+    // lower-triangle tiles: row tile a (16 rows) x column tiles 0 .. 2a+1 (8 columns)
+    for (int tix = warp; tix < (C / 16) * (C / 16 + 1); tix += kWarps) {
+      int a = 0, rem = tix;
+      while (rem >= 2 * a + 2) {
+        rem -= 2 * a + 2;
+        ++a;
+      }
+      const int m0 = 16 * a, n0 = 8 * rem;
+      float d[4];
+      tile<true>(d, X, xl, Y, xl, m0, n0, nk);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = m0 + gq + 8 * (e >> 1), j = n0 + 2 * tq + (e & 1);
+        out[i * lo + j] = (below(i, j) && i < Lc) ? (s ? s[i] : 1.f) * expf(gam[i] - gam[j]) * d[e] : 0.f;
+      }
+    }
+    __syncthreads();
+    return;
+  }
+  const bool factored = gram_factored(K);
+  const int per_row = factored ? 16 : C;
+  for (int p = warp; p < C * per_row; p += kWarps) {
+    const int i = p / per_row, j = (factored ? 16 * (i / 16) : 0) + p % per_row;
+    if (!below(i, j) || i >= Lc) {
+      if (lane == 0) out[i * lo + j] = 0.f;
+      continue;
+    }
+    float acc = 0.f;
+    for (int64_t d = lane; d < K; d += 32)
+      acc = fmaf(X[i * xl + d] * Y[j * xl + d], expf(gam[i * gl + d] - gam[j * gl + d]), acc);
+    acc = warp_sum(acc);
+    if (lane == 0) out[i * lo + j] = (s ? s[i] : 1.f) * acc;
+  }
+  for (int a = 1; factored && a < C / 16; ++a) {
+    const int r = 16 * a;
+    __syncthreads();
+    for (int64_t e = tid; e < (16 + r) * Kp; e += 256) {
+      const int row = (int)(e / Kp);
+      const int64_t d = e % Kp;
+      if (row < 16) {
+        const int i = r + row;
+        Xs[row * xl + d] = d < K ? X[i * xl + d] * expf(gam[i * gl + d] - gam[r * gl + d]) : 0.f;
+      } else {
+        const int jr = row - 16;
+        Ys[jr * xl + d] = d < K ? Y[jr * xl + d] * expf(gam[r * gl + d] - gam[jr * gl + d]) : 0.f;
+      }
+    }
+    __syncthreads();
+    for (int nt = warp; nt < r / 8; nt += kWarps) {
+      float d[4];
+      tile<true>(d, Xs, xl, Ys, xl, 0, 8 * nt, nk);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = r + gq + 8 * (e >> 1), j = 8 * nt + 2 * tq + (e & 1);
+        out[i * lo + j] = i < Lc ? (s ? s[i] : 1.f) * d[e] : 0.f;
+      }
+    }
+  }
+  __syncthreads();
+}
+
 }  // namespace prep
 }  // namespace gdr
