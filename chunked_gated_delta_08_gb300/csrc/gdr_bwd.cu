@@ -29,6 +29,8 @@
 // forward's chunk layouts and int64 addressing; it supports K <= 128.
 #include "gdr_device.cuh"
 #include "gdr_internal.h"
+#include "gdr_prep.cuh"
+#include "gdr_scan.cuh"
 
 namespace gdr {
 namespace {
@@ -73,73 +75,80 @@ __device__ __forceinline__ void load_gamma(const float *__restrict__ gcum, int64
 }
 
 // --------------------------------------------------------------------------
-// dv_local: dv_new (local part) = P^T do.  grid (nt_max, HV).
-// smem: qs[C*K] | ks[C*K] | gam[C*K or C] | P[C*C] | dos[C*C]
+// dv_local: dv_new (local part) = P^T do.  grid (nt_max, HV).  P from
+// prep::decayed_gram, then one tensor-core product (3 x TF32) per 32-column
+// V tile.
+// smem: qs[C][KL] | ks[C][KL] | gam | P[C][C+4] | dos[C][40] | Xs, Ys
 // --------------------------------------------------------------------------
+constexpr int kDvLd = 40;
+
+__host__ __device__ constexpr int64_t dv_local_smem_floats(int C, int64_t K, bool per_k) {
+  return 2 * C * (scan::kpad(K) + 4) + (per_k ? C * scan::kpad(K) : C) + C * (C + 4) + C * kDvLd +
+         prep::gram_scratch_floats(C, K, per_k);
+}
+
 template <typename Tin, int C, bool PER_K>
 __global__ void __launch_bounds__(kThreads) bwd_dv_local_kernel(
     const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ d_o,
     const float *__restrict__ gcum, const int64_t *__restrict__ cu, const int64_t *__restrict__ chunk_indices,
     int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V, int l2, float *__restrict__ dvn) {
   extern __shared__ float smem[];
+  const int64_t Kp = scan::kpad(K), KL = Kp + 4, GL = PER_K ? Kp : 1;
+  constexpr int LP = C + 4;
   float *qs = smem;
-  float *ks = qs + C * K;
-  float *gam = ks + C * K;
-  float *P = gam + (PER_K ? C * K : C);
-  float *dos = P + C * C;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float *ks = qs + C * KL;
+  float *gam = ks + C * KL;
+  float *P = gam + (PER_K ? C * Kp : C);
+  float *dos = P + C * LP;
+  float *Xs = dos + C * kDvLd;
+  float *Ys = Xs + 16 * KL;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, gq = lane >> 2, tq = lane & 3;
   const int64_t hv = blockIdx.y;
   ChunkPos cp;
   if (!chunk_pos(cu, chunk_indices, blockIdx.x, T, C, &cp)) return;
   const int64_t t0 = cp.t0;
   const int Lc = cp.Lc;
   const int64_t hq = hv / (HV / H);
+  const int64_t gw = PER_K ? K : 1;
 
-  for (int i = warp; i < C; i += kWarps) {
-    load_row_normed(q, t0 + i, H, hq, K, i < Lc, l2, qs + i * K, lane);
-    load_row_normed(k, t0 + i, H, hq, K, i < Lc, l2, ks + i * K, lane);
+  prep::load_qk_rows<Tin, C>(q, k, t0, Lc, H, hq, K, l2, qs, ks, KL);
+  for (int64_t e = tid; e < C * gw; e += kThreads) {
+    const int64_t i = e / gw, d = e % gw;
+    gam[i * GL + d] = i < Lc ? gcum[((t0 + i) * HV + hv) * gw + d] : 0.f;
   }
-  load_gamma<PER_K>(gcum, t0, Lc, C, HV, hv, K, gam, tid);
+  for (int e = tid; e < C * LP; e += kThreads) P[e] = 0.f;  // P^T reads the upper part
   __syncthreads();
   // P_ri = sum_d q_rd k_id exp(G_rd - G_id), i <= r < Lc
-  for (int p = warp; p < C * C; p += kWarps) {
-    const int r = p / C, i = p % C;
-    if (i > r || r >= Lc) {
-      if (lane == 0) P[p] = 0.f;
-      continue;
-    }
-    float s = 0.f;
-    for (int64_t d = lane; d < K; d += 32) {
-      float t = qs[r * K + d] * ks[i * K + d];
-      if (PER_K) t *= expf(gam[r * K + d] - gam[i * K + d]);
-      s += t;
-    }
-    s = warp_sum(s);
-    if (lane == 0) P[p] = s * (PER_K ? 1.f : expf(gam[r] - gam[i]));
-  }
-  __syncthreads();
-  for (int64_t v0 = 0; v0 < V; v0 += C) {
-    for (int e = tid; e < C * C; e += kThreads) {
-      const int r = e / C, vv = e % C;
-      dos[e] = (r < Lc && v0 + vv < V) ? to_f32(d_o[((t0 + r) * HV + hv) * V + v0 + vv]) : 0.f;
+  prep::decayed_gram<C, PER_K, false>(qs, ks, KL, gam, GL, K, Lc, nullptr, P, LP, Xs, Ys);
+  for (int64_t v0 = 0; v0 < V; v0 += 32) {
+    __syncthreads();
+    for (int e = tid; e < C * 32; e += kThreads) {
+      const int r = e / 32, vv = e % 32;
+      dos[r * kDvLd + vv] = (r < Lc && v0 + vv < V) ? to_f32(d_o[((t0 + r) * HV + hv) * V + v0 + vv]) : 0.f;
     }
     __syncthreads();
-    for (int e = tid; e < C * C; e += kThreads) {
-      const int i = e / C, vv = e % C;
-      if (i < Lc && v0 + vv < V) {
-        float acc = 0.f;
-        for (int r = i; r < Lc; ++r) acc = fmaf(P[r * C + i], dos[r * C + vv], acc);
-        dvn[((t0 + i) * HV + hv) * V + v0 + vv] = acc;
+    for (int tix = warp; tix < (C / 16) * 4; tix += kWarps) {
+      const int m0 = 16 * (tix % (C / 16)), n0 = 8 * (tix / (C / 16));
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      prep::tile_acc<true, false>(d, P, LP, dos, kDvLd, m0, n0, C / 8);  // A(i, r) = P[r][i]
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = m0 + gq + 8 * (e >> 1);
+        const int64_t col = v0 + n0 + 2 * tq + (e & 1);
+        if (i < Lc && col < V) dvn[((t0 + i) * HV + hv) * V + col] = d[e];
       }
     }
-    __syncthreads();
   }
 }
 
 // --------------------------------------------------------------------------
 // dh: grid (N, HV, ceil(V / 32)), sequential over the sequence's chunks, last
-// to first.  Completes dv_new (adds Kb dh') and records dh' per chunk.
-// smem: dh[K*32] | kb[C*K] (Kb, then Qt) | ws[C*K] | dos[C*32] | dvs[C*32] | gl[K]
+// to first.  Per chunk, on tensor cores (3 x TF32):
+//   dv_new += Kb dh'           (C x 32) = (C x K)(K x 32), Kb = k e^{G_L - G}
+//   dh = e^{G_L} dh' + Qt^T do - w^T dv_new   (K x 32),      Qt = q e^G
+// and dh' (dL/d state leaving the chunk) is recorded per chunk.
+// smem: the scan tiles (dh in hs, Kb then Qt in kt, -w in ws, dv_new in vn,
+//       G_L in gl) | dos[C][40]
 // --------------------------------------------------------------------------
 template <typename Tin, int C, bool PER_K>
 __global__ void __launch_bounds__(kThreads) bwd_dh_kernel(
@@ -149,24 +158,22 @@ __global__ void __launch_bounds__(kThreads) bwd_dh_kernel(
     int64_t HV, int64_t K, int64_t V, int l2, float *__restrict__ dvn, float *__restrict__ dhc,
     float *__restrict__ dh0) {
   extern __shared__ float smem[];
-  float *dh = smem;
-  float *kb = dh + K * kBVd;
-  float *ws = kb + C * K;
-  float *dos = ws + C * K;
-  float *dvs = dos + C * kBVd;
-  float *gl = dvs + C * kBVd;
+  const scan::Tiles st = scan::carve(smem, C, K);
+  float *dos = smem + scan::smem_floats(C, K);
   if (chunk_offsets && chunk_offsets[N] < 0) return;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, gq = lane >> 2, tq = lane & 3;
   const int64_t n = blockIdx.x, hv = blockIdx.y, v0 = (int64_t)blockIdx.z * kBVd;
   const int64_t hq = hv / (HV / H);
+  const int64_t Kp = scan::kpad(K), WL = scan::ws_ld(K), KL = scan::kt_ld(K);
   const SeqRange sr = seq_range(cu, n, T);
   const int64_t nch = (sr.eos - sr.bos + C - 1) / C;
   const int64_t cbase = chunk_offsets ? chunk_offsets[n] : n * ((T + C - 1) / C);
   const int64_t gw = PER_K ? K : 1;
+  constexpr int LD = scan::kHS;
 
-  for (int64_t e = tid; e < K * kBVd; e += kThreads) {
+  for (int64_t e = tid; e < Kp * kBVd; e += kThreads) {
     const int64_t d = e / kBVd, vv = e % kBVd;
-    dh[e] = (dht && v0 + vv < V) ? dht[((n * HV + hv) * K + d) * V + v0 + vv] : 0.f;
+    st.hs[d * LD + vv] = (dht && d < K && v0 + vv < V) ? dht[((n * HV + hv) * K + d) * V + v0 + vv] : 0.f;
   }
   __syncthreads();
 
@@ -176,62 +183,74 @@ __global__ void __launch_bounds__(kThreads) bwd_dh_kernel(
     const int64_t tl = t0 + Lc - 1;
     for (int64_t e = tid; e < K * kBVd; e += kThreads) {
       const int64_t d = e / kBVd, vv = e % kBVd;
-      if (v0 + vv < V) dhc[(((cbase + c) * HV + hv) * K + d) * V + v0 + vv] = dh[e];
+      if (v0 + vv < V) dhc[(((cbase + c) * HV + hv) * K + d) * V + v0 + vv] = st.hs[d * LD + vv];
     }
-    for (int64_t d = tid; d < K; d += kThreads) gl[d] = gcum[(tl * HV + hv) * gw + (PER_K ? d : 0)];
+    for (int64_t d = tid; d < Kp; d += kThreads)
+      st.gl[d] = d < K ? gcum[(tl * HV + hv) * gw + (PER_K ? d : 0)] : 0.f;
     __syncthreads();
-    // Kb_id = k_id exp(G_Ld - G_id)
-    for (int i = warp; i < C; i += kWarps) {
-      load_row_normed(k, t0 + i, H, hq, K, i < Lc, l2, kb + i * K, lane);
-      for (int64_t d = lane; d < K; d += 32) {
-        const float gi = i < Lc ? gcum[((t0 + i) * HV + hv) * gw + (PER_K ? d : 0)] : 0.f;
-        kb[i * K + d] *= (i < Lc) ? expf(gl[d] - gi) : 0.f;
-      }
-    }
+    // Kb into kt, -w into ws
+    if (K <= 128) scan::load_rows<Tin, C, PER_K, 4, 4>(st, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
+    else scan::load_rows<Tin, C, PER_K, 8, 2>(st, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
     __syncthreads();
     // dv_new += Kb dh'
-    for (int e = tid; e < C * kBVd; e += kThreads) {
-      const int i = e / kBVd, vv = e % kBVd;
-      float acc = 0.f;
-      if (i < Lc && v0 + vv < V) {
-        float *dst = dvn + ((t0 + i) * HV + hv) * V + v0 + vv;
-        acc = *dst;
-        for (int64_t d = 0; d < K; ++d) acc = fmaf(kb[i * K + d], dh[d * kBVd + vv], acc);
-        *dst = acc;
+    for (int tix = warp; tix < (C / 16) * 4; tix += kWarps) {
+      const int m0 = 16 * (tix % (C / 16)), n0 = 8 * (tix / (C / 16));
+      float d[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = m0 + gq + 8 * (e >> 1);
+        const int64_t col = v0 + n0 + 2 * tq + (e & 1);
+        d[e] = (i < Lc && col < V) ? dvn[((t0 + i) * HV + hv) * V + col] : 0.f;
       }
-      dvs[e] = acc;
+      prep::tile_acc<false, false>(d, st.kt, KL, st.hs, LD, m0, n0, (int)(Kp / 8));
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = m0 + gq + 8 * (e >> 1), cc = n0 + 2 * tq + (e & 1);
+        const int64_t col = v0 + cc;
+        if (i < Lc && col < V) dvn[((t0 + i) * HV + hv) * V + col] = d[e];
+        st.vn[i * LD + cc] = d[e];
+      }
     }
     __syncthreads();
-    // Qt_id = q_id exp(G_id); w; do
-    for (int i = warp; i < C; i += kWarps) {
-      load_row_normed(q, t0 + i, H, hq, K, i < Lc, l2, kb + i * K, lane);
-      for (int64_t d = lane; d < K; d += 32) {
-        const float gi = i < Lc ? gcum[((t0 + i) * HV + hv) * gw + (PER_K ? d : 0)] : 0.f;
-        kb[i * K + d] *= (i < Lc) ? expf(gi) : 0.f;
-        ws[i * K + d] = i < Lc ? w[((t0 + i) * HV + hv) * K + d] : 0.f;
-      }
-    }
+    // Qt into kt (over Kb), do into dos
+    prep::load_qk_rows<Tin, C>(nullptr, q, t0, Lc, H, hq, K, l2, nullptr, st.kt, KL);
     for (int e = tid; e < C * kBVd; e += kThreads) {
       const int i = e / kBVd, vv = e % kBVd;
-      dos[e] = (i < Lc && v0 + vv < V) ? to_f32(d_o[((t0 + i) * HV + hv) * V + v0 + vv]) : 0.f;
+      dos[i * LD + vv] = (i < Lc && v0 + vv < V) ? to_f32(d_o[((t0 + i) * HV + hv) * V + v0 + vv]) : 0.f;
     }
     __syncthreads();
-    // dh <- exp(G_L) dh' + Qt^T do - w^T dv_new
-    for (int64_t e = tid; e < K * kBVd; e += kThreads) {
-      const int64_t d = e / kBVd, vv = e % kBVd;
-      float acc = dh[e] * expf(gl[d]);
-      for (int i = 0; i < Lc; ++i) {
-        acc = fmaf(kb[i * K + d], dos[i * kBVd + vv], acc);
-        acc = fmaf(-ws[i * K + d], dvs[i * kBVd + vv], acc);
+    for (int64_t e = tid; e < C * Kp; e += kThreads) {
+      const int i = (int)(e / Kp);
+      const int64_t d = e % Kp;
+      if (i < Lc && d < K) st.kt[i * KL + d] *= expf(gcum[((t0 + i) * HV + hv) * gw + (PER_K ? d : 0)]);
+    }
+    __syncthreads();
+    // dh = e^{G_L} dh' + Qt^T do - w^T dv_new
+    for (int tix = warp; tix < (int)(Kp / 16) * 4; tix += kWarps) {
+      const int m0 = 16 * (tix % (int)(Kp / 16)), n0 = 8 * (tix / (int)(Kp / 16));
+      float d[4];
+      const float e0 = expf(st.gl[PER_K ? m0 + gq : 0]), e1 = expf(st.gl[PER_K ? m0 + gq + 8 : 0]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = m0 + gq + 8 * (e >> 1), cc = n0 + 2 * tq + (e & 1);
+        d[e] = st.hs[r * LD + cc] * ((e >> 1) ? e1 : e0);
       }
-      dh[e] = acc;
+      prep::tile_acc<true, false>(d, st.kt, KL, dos, LD, m0, n0, C / 8);
+      prep::tile_acc<true, false>(d, st.ws, WL, st.vn, LD, m0, n0, C / 8);
+      __syncwarp();
+      // every warp reads only its own tiles of hs, so the write-back needs no barrier
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = m0 + gq + 8 * (e >> 1), cc = n0 + 2 * tq + (e & 1);
+        st.hs[r * LD + cc] = d[e];
+      }
     }
     __syncthreads();
   }
   if (dh0)
     for (int64_t e = tid; e < K * kBVd; e += kThreads) {
       const int64_t d = e / kBVd, vv = e % kBVd;
-      if (v0 + vv < V) dh0[((n * HV + hv) * K + d) * V + v0 + vv] = dh[e];
+      if (v0 + vv < V) dh0[((n * HV + hv) * K + d) * V + v0 + vv] = st.hs[d * LD + vv];
     }
 }
 
@@ -708,7 +727,7 @@ int launch_bwd_dv_local(const BwdArgs &a) {
     constexpr int C = decltype(cfg)::C;
     constexpr bool PK = decltype(cfg)::PK;
     const int64_t K = f.d.K;
-    const size_t smem = sizeof(float) * (2 * C * K + (PK ? C * K : C) + 2 * C * C);
+    const size_t smem = sizeof(float) * dv_local_smem_floats(C, K, PK);
     auto kern = bwd_dv_local_kernel<Tin, C, PK>;
     int rc = set_smem(kern, smem, "bwd_dv_local_kernel");
     if (rc != GDR_OK) return rc;
@@ -727,7 +746,7 @@ int launch_bwd_dh(const BwdArgs &a) {
     constexpr int C = decltype(cfg)::C;
     constexpr bool PK = decltype(cfg)::PK;
     const int64_t K = f.d.K;
-    const size_t smem = sizeof(float) * (K * kBVd + 2 * C * K + 2 * C * kBVd + K);
+    const size_t smem = sizeof(float) * (scan::smem_floats(C, K) + C * scan::kHS);
     auto kern = bwd_dh_kernel<Tin, C, PK>;
     int rc = set_smem(kern, smem, "bwd_dh_kernel");
     if (rc != GDR_OK) return rc;

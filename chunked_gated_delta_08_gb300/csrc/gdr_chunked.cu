@@ -336,41 +336,7 @@ __global__ void __launch_bounds__(kThreads) fwd_o_kernel(
   const int64_t hq = hv / (HV / H);
   const int64_t gw = PER_K ? K : 1;
 
-  // q and k rows (normalized), four rows per warp in flight at a time
-  for (int i0 = warp; i0 < C; i0 += 4 * kWarps) {
-    float qv[4][8], kv[4][8];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int i = i0 + kWarps * r;
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int64_t d = lane + 32 * m;
-        const bool ok = i < C && i < Lc && d < K;
-        qv[r][m] = ok ? to_f32(q[((t0 + i) * H + hq) * K + d]) : 0.f;
-        kv[r][m] = ok ? to_f32(k[((t0 + i) * H + hq) * K + d]) : 0.f;
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int i = i0 + kWarps * r;
-      if (i >= C) break;
-      float sq = 0.f, sk = 0.f;
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        sq = fmaf(qv[r][m], qv[r][m], sq);
-        sk = fmaf(kv[r][m], kv[r][m], sk);
-      }
-      const float cq = l2 ? rsqrtf(warp_sum(sq) + kL2Eps) : 1.f, ck = l2 ? rsqrtf(warp_sum(sk) + kL2Eps) : 1.f;
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int64_t d = lane + 32 * m;
-        if (d < KL) {
-          qs[i * KL + d] = qv[r][m] * cq;
-          ks[i * KL + d] = kv[r][m] * ck;
-        }
-      }
-    }
-  }
+  prep::load_qk_rows<Tin, C>(q, k, t0, Lc, H, hq, K, l2, qs, ks, KL);
   for (int64_t e = tid; e < C * gw; e += kThreads) {
     const int64_t i = e / gw, d = e % gw;
     gam[i * GL + d] = i < Lc ? gcum[((t0 + i) * HV + hv) * gw + d] : 0.f;

@@ -44,6 +44,41 @@ __device__ __forceinline__ void tile(float (&d)[4], const float *a, int64_t lda,
   }
 }
 
+// d += sum over k < 8 nk of A(m, k) B(k, n) on the 16 x 8 tile at (m0, n0):
+// A(m, k) = TA ? a[k lda + m] : a[m lda + k];  B(k, n) = TB ? b[n ldb + k] : b[k ldb + n].
+template <bool TA, bool TB>
+__device__ __forceinline__ void tile_acc(float (&d)[4], const float *a, int64_t lda, const float *b, int64_t ldb,
+                                         int m0, int n0, int nk) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  for (int ks = 0; ks < nk; ++ks) {
+    const int k0 = 8 * ks;
+    uint32_t ah[4], al[4], bh[2], bl[2];
+    if (TA) {
+      const float *ar = a + (int64_t)(k0 + t) * lda + m0 + g;
+      scan::split3(ar[0], ah[0], al[0]);
+      scan::split3(ar[8], ah[1], al[1]);
+      scan::split3(ar[4 * lda], ah[2], al[2]);
+      scan::split3(ar[4 * lda + 8], ah[3], al[3]);
+    } else {
+      const float *ar = a + (int64_t)(m0 + g) * lda + k0 + t;
+      scan::split3(ar[0], ah[0], al[0]);
+      scan::split3(ar[8 * lda], ah[1], al[1]);
+      scan::split3(ar[4], ah[2], al[2]);
+      scan::split3(ar[8 * lda + 4], ah[3], al[3]);
+    }
+    if (TB) {
+      const float *br = b + (int64_t)(n0 + g) * ldb + k0 + t;
+      scan::split3(br[0], bh[0], bl[0]);
+      scan::split3(br[4], bh[1], bl[1]);
+    } else {
+      const float *br = b + (int64_t)(k0 + t) * ldb + n0 + g;
+      scan::split3(br[0], bh[0], bl[0]);
+      scan::split3(br[4 * ldb], bh[1], bl[1]);
+    }
+    scan::mma3(d, ah, al, bh, bl);
+  }
+}
+
 // The same with A and B read through functors fa(m, k), fb(k, n) (tile-local
 // indices), for the triangular operands of the solve.
 template <typename FA, typename FB>
@@ -148,6 +183,52 @@ __device__ void solve_unit_lower(float *AT, int lda, float *X) {
       AT[(cc + 1) * lda + rr + 8] = -d[3];
     }
     __syncthreads();
+  }
+}
+
+// Rows of q (optional) and k, L2-normalized if asked, zero past Lc and past K,
+// into qs and ks (row stride xl >= kpad(K) + 4).  Four rows per warp have
+// their loads in flight before any row is reduced.  All 256 threads.
+template <typename Tin, int C>
+__device__ __forceinline__ void load_qk_rows(const Tin *__restrict__ q, const Tin *__restrict__ k, int64_t t0,
+                                             int Lc, int64_t H, int64_t hq, int64_t K, int l2, float *qs,
+                                             float *ks, int64_t xl) {
+  constexpr int kWarps = 8;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t width = scan::kpad(K) + 4;
+  for (int i0 = warp; i0 < C; i0 += 4 * kWarps) {
+    float qv[4][8], kv[4][8];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = i0 + kWarps * r;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int64_t d = lane + 32 * m;
+        const bool ok = i < C && i < Lc && d < K;
+        qv[r][m] = (q && ok) ? to_f32(q[((t0 + i) * H + hq) * K + d]) : 0.f;
+        kv[r][m] = ok ? to_f32(k[((t0 + i) * H + hq) * K + d]) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = i0 + kWarps * r;
+      if (i >= C) break;
+      float sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        sq = fmaf(qv[r][m], qv[r][m], sq);
+        sk = fmaf(kv[r][m], kv[r][m], sk);
+      }
+      const float cq = l2 ? rsqrtf(warp_sum(sq) + kL2Eps) : 1.f, ck = l2 ? rsqrtf(warp_sum(sk) + kL2Eps) : 1.f;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int64_t d = lane + 32 * m;
+        if (d < width) {
+          if (q) qs[i * xl + d] = qv[r][m] * cq;
+          ks[i * xl + d] = kv[r][m] * ck;
+        }
+      }
+    }
   }
 }
 
