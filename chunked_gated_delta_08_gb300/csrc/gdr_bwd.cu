@@ -38,7 +38,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBVd = 32;   // V-tile of the dh scan
-constexpr int kVt = 32;    // V-tile of the dq/dk/dgamma accumulation
 constexpr int kTw = 128;   // column tile of the triangular back substitution
 constexpr int kKmax = 128; // largest K of the backward
 
@@ -256,14 +255,21 @@ __global__ void __launch_bounds__(kThreads) bwd_dh_kernel(
 
 // --------------------------------------------------------------------------
 // dqkg: grid (nt_max, HV).  Accumulates dQt = do h^T, dW = -dv_new h^T,
-// dKb = v_new dh'^T, dP = do v_new^T over V tiles, then forms the chunk's
-// dq^, dk^ and dGamma from the output and state terms.
-// Thread t owns column d = t % 128 and rows i = 2m + t / 128 of every C x K
-// accumulator, and entries (r, i) = (m (256 / C) + t / C, t % C) of dP.
-// smem: qs[C*K] | ks[C*K] | gam[C*K or C] | doT, dvT, vnT [kVt*(C+1)] |
-//       hT, dhT [kVt*(K+1)] | dPs[C*C] | colsum[2*128] | gLs[K]
-// (the V tiles are reused as the scalar gate's per-element dGamma, C*K)
+// dKb = v_new dh'^T, dP = do v_new^T over 32-column V tiles on tensor cores
+// (3 x TF32, accumulators in registers), then forms the chunk's dq^, dk^ and
+// dGamma from the output and state terms on CUDA cores, where thread t owns
+// column d = t % 128 and rows i = 2m + t / 128 of every C x K matrix.
+// smem: qs[C*K] | ks[C*K] | gam[C*K or C] | tiles (do, dv_new, v_new [C][36],
+//       h, dh' [Kp][36]; then the staged dQt, dKb [C][Kp]; then the scalar
+//       gate's per-element dGamma) | dPs[C*C] | colsum[2*128] | gLs[K]
 // --------------------------------------------------------------------------
+constexpr int kQL = 36;  // row stride of the V tiles (4 mod 32)
+
+__host__ __device__ constexpr int64_t dqkg_region_floats(int C, int64_t K) {
+  return (3 * C + 2 * scan::kpad(K)) * kQL > 2 * C * scan::kpad(K) ? (3 * C + 2 * scan::kpad(K)) * kQL
+                                                                     : 2 * C * scan::kpad(K);
+}
+
 template <typename Tin, int C, bool PER_K>
 __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
     const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ d_o,
@@ -271,23 +277,24 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
     const float *__restrict__ dhc, const float *__restrict__ gcum, const int64_t *__restrict__ cu,
     const int64_t *__restrict__ chunk_indices, int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V, int l2,
     float *__restrict__ dqa, float *__restrict__ dka, float *__restrict__ dga, float *__restrict__ dW) {
-  constexpr int MQ = C * kKmax / kThreads;  // rows per thread
-  constexpr int MP = C * C / kThreads;      // dP entries per thread
-  constexpr int PR = kThreads / C;          // dP rows covered per m
+  constexpr int MQ = C * kKmax / kThreads;  // rows per thread in the per-element phase
+  constexpr int MT = C / 16;                // row tiles
+  constexpr int NTW = 16 * MT / 8;          // column tiles of a C x 128 product per warp
+  constexpr int NPW = MT * (C / 8) / 8;     // tiles of dP per warp
   extern __shared__ float smem[];
+  const int64_t Kp = scan::kpad(K);
   float *qs = smem;
   float *ks = qs + C * K;
   float *gam = ks + C * K;
-  float *doT = gam + (PER_K ? C * K : C);
-  float *dvT = doT + kVt * (C + 1);
-  float *vnT = dvT + kVt * (C + 1);
-  float *hT = vnT + kVt * (C + 1);
-  float *dhT = hT + kVt * (K + 1);
-  float *dPs = dhT + kVt * (K + 1);
+  float *reg = gam + (PER_K ? C * K : C);
+  float *doA = reg, *dvA = doA + C * kQL, *vnA = dvA + C * kQL;
+  float *hB = vnA + C * kQL, *dhB = hB + Kp * kQL;
+  float *sQ = reg, *sK = reg + C * Kp;  // after the V loop
+  float *rowbuf = reg;                  // after sQ, sK are read
+  float *dPs = reg + dqkg_region_floats(C, K);
   float *colsum = dPs + C * C;
   float *gLs = colsum + 2 * kKmax;
-  float *rowbuf = doT;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, gq = lane >> 2, tq = lane & 3;
   const int64_t chunk = blockIdx.x, hv = blockIdx.y;
   ChunkPos cp;
   if (!chunk_pos(cu, chunk_indices, chunk, T, C, &cp)) return;
@@ -295,7 +302,8 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
   const int Lc = cp.Lc;
   const int64_t hq = hv / (HV / H);
   const int d = tid & (kKmax - 1), i_base = tid / kKmax;
-  const int pi = tid % C, pr_base = tid / C;
+  const int ntk = (int)(Kp / 8);  // column tiles of a C x Kp product
+  const int m0 = 16 * (warp % MT);
 
   for (int i = warp; i < C; i += kWarps) {
     load_row_normed(q, t0 + i, H, hq, K, i < Lc, l2, qs + i * K, lane);
@@ -304,51 +312,113 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
   load_gamma<PER_K>(gcum, t0, Lc, C, HV, hv, K, gam, tid);
   for (int e = tid; e < 2 * kKmax; e += kThreads) colsum[e] = 0.f;
 
-  float aQ[MQ], aW[MQ], aK[MQ], aP[MP];
+  float aQ[MQ], aW[MQ], aK[MQ];
+  float fQ[NTW][4], fW[NTW][4], fK[NTW][4], fP[NPW][4];
 #pragma unroll
-  for (int m = 0; m < MQ; ++m) aQ[m] = aW[m] = aK[m] = 0.f;
+  for (int s = 0; s < NTW; ++s)
 #pragma unroll
-  for (int m = 0; m < MP; ++m) aP[m] = 0.f;
+    for (int e = 0; e < 4; ++e) fQ[s][e] = fW[s][e] = fK[s][e] = 0.f;
+#pragma unroll
+  for (int s = 0; s < NPW; ++s)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) fP[s][e] = 0.f;
   float gLacc = 0.f;
 
-  for (int64_t v0 = 0; v0 < V; v0 += kVt) {
-    for (int e = tid; e < C * kVt; e += kThreads) {
-      const int r = e / kVt, vv = e % kVt;
+  for (int64_t v0 = 0; v0 < V; v0 += 32) {
+    __syncthreads();  // the previous tile's reads are done
+    for (int e = tid; e < C * 32; e += kThreads) {
+      const int r = e / 32, vv = e % 32;
       const bool ok = r < Lc && v0 + vv < V;
       const int64_t g = ((t0 + r) * HV + hv) * V + v0 + vv;
-      doT[vv * (C + 1) + r] = ok ? to_f32(d_o[g]) : 0.f;
-      dvT[vv * (C + 1) + r] = ok ? dvn[g] : 0.f;
-      vnT[vv * (C + 1) + r] = ok ? v_new[g] : 0.f;
+      doA[r * kQL + vv] = ok ? to_f32(d_o[g]) : 0.f;
+      dvA[r * kQL + vv] = ok ? -dvn[g] : 0.f;
+      vnA[r * kQL + vv] = ok ? v_new[g] : 0.f;
     }
-    for (int64_t e = tid; e < K * kVt; e += kThreads) {
-      const int64_t dd = e / kVt, vv = e % kVt;
-      const bool ok = v0 + vv < V;
+    for (int64_t e = tid; e < Kp * 32; e += kThreads) {
+      const int64_t dd = e / 32, vv = e % 32;
+      const bool ok = dd < K && v0 + vv < V;
       const int64_t g = ((chunk * HV + hv) * K + dd) * V + v0 + vv;
-      hT[vv * (K + 1) + dd] = ok ? h[g] : 0.f;
-      dhT[vv * (K + 1) + dd] = ok ? dhc[g] : 0.f;
+      hB[dd * kQL + vv] = ok ? h[g] : 0.f;
+      dhB[dd * kQL + vv] = ok ? dhc[g] : 0.f;
     }
     __syncthreads();
-    if (d < K) {
-      for (int vv = 0; vv < kVt; ++vv) {
-        const float hv_ = hT[vv * (K + 1) + d], dh_ = dhT[vv * (K + 1) + d];
-        const float *dor = doT + vv * (C + 1), *dvr = dvT + vv * (C + 1), *vnr = vnT + vv * (C + 1);
+    if (tid < K)
+      for (int vv = 0; vv < 32; ++vv) gLacc = fmaf(hB[tid * kQL + vv], dhB[tid * kQL + vv], gLacc);
 #pragma unroll
-        for (int m = 0; m < MQ; ++m) {
-          const int i = 2 * m + i_base;
-          aQ[m] = fmaf(dor[i], hv_, aQ[m]);
-          aW[m] = fmaf(-dvr[i], hv_, aW[m]);
-          aK[m] = fmaf(vnr[i], dh_, aK[m]);
+    for (int k0 = 0; k0 < 32; k0 += 8) {
+      uint32_t oh[4], ol[4], wh[4], wl[4], nh[4], nl[4];
+      {
+        const float *ar = doA + (m0 + gq) * kQL + k0 + tq;
+        const float *br = dvA + (m0 + gq) * kQL + k0 + tq;
+        const float *cr = vnA + (m0 + gq) * kQL + k0 + tq;
+        const int offs[4] = {0, 8 * kQL, 4, 8 * kQL + 4};
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          scan::split3(ar[offs[x]], oh[x], ol[x]);
+          scan::split3(br[offs[x]], wh[x], wl[x]);
+          scan::split3(cr[offs[x]], nh[x], nl[x]);
         }
-        if (tid < K) gLacc = fmaf(hv_, dh_, gLacc);
+      }
+#pragma unroll
+      for (int s = 0; s < NTW; ++s) {
+        const int tix = warp + 8 * s;  // m-tile tix % MT (fixed per warp), n-tile tix / MT
+        const int n0 = 8 * (tix / MT);
+        if (n0 >= 8 * ntk) continue;
+        uint32_t bh[2], bl[2], ch[2], cl[2];
+        const float *hb = hB + (n0 + gq) * kQL + k0 + tq;
+        const float *db = dhB + (n0 + gq) * kQL + k0 + tq;
+        scan::split3(hb[0], bh[0], bl[0]);
+        scan::split3(hb[4], bh[1], bl[1]);
+        scan::split3(db[0], ch[0], cl[0]);
+        scan::split3(db[4], ch[1], cl[1]);
+        scan::mma3(fQ[s], oh, ol, bh, bl);
+        scan::mma3(fW[s], wh, wl, bh, bl);
+        scan::mma3(fK[s], nh, nl, ch, cl);
+      }
+#pragma unroll
+      for (int s = 0; s < NPW; ++s) {
+        const int n0 = 8 * ((warp + 8 * s) / MT);
+        uint32_t bh[2], bl[2];
+        const float *vb = vnA + (n0 + gq) * kQL + k0 + tq;
+        scan::split3(vb[0], bh[0], bl[0]);
+        scan::split3(vb[4], bh[1], bl[1]);
+        scan::mma3(fP[s], oh, ol, bh, bl);
       }
     }
-    for (int vv = 0; vv < kVt; ++vv) {
-      const float vn_i = vnT[vv * (C + 1) + pi];
-#pragma unroll
-      for (int m = 0; m < MP; ++m) aP[m] = fmaf(doT[vv * (C + 1) + m * PR + pr_base], vn_i, aP[m]);
-    }
-    __syncthreads();
   }
+  __syncthreads();  // the V tiles are dead: stage dQt and dKb, write dW, stage dP
+#pragma unroll
+  for (int s = 0; s < NTW; ++s) {
+    const int n0 = 8 * ((warp + 8 * s) / MT);
+    if (n0 >= 8 * ntk) continue;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = m0 + gq + 8 * (e >> 1), dd = n0 + 2 * tq + (e & 1);
+      sQ[i * Kp + dd] = fQ[s][e];
+      sK[i * Kp + dd] = fK[s][e];
+      if (i < Lc && dd < K) dW[((t0 + i) * HV + hv) * K + dd] = fW[s][e];
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < NPW; ++s) {
+    const int n0 = 8 * ((warp + 8 * s) / MT);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int r = m0 + gq + 8 * (e >> 1), i = n0 + 2 * tq + (e & 1);
+      float val = 0.f;
+      if (r < Lc && i <= r) val = PER_K ? fP[s][e] : fP[s][e] * expf(gam[r] - gam[i]);
+      dPs[r * C + i] = val;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int m = 0; m < MQ; ++m) {
+    const int i = 2 * m + i_base;
+    aQ[m] = d < K ? sQ[i * Kp + d] : 0.f;
+    aK[m] = d < K ? sK[i * Kp + d] : 0.f;
+    aW[m] = 0.f;
+  }
+  __syncthreads();  // rowbuf may now reuse the staging
 
   // dW out; dP staged (GDN folds its decay in); column sums of dKb * Kb,
   // each thread's half in a fixed slot so the sum's order is fixed
@@ -358,7 +428,6 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
     for (int m = 0; m < MQ; ++m) {
       const int i = 2 * m + i_base;
       if (i < Lc) {
-        dW[((t0 + i) * HV + hv) * K + d] = aW[m];
         const float gi = gam_at<PER_K>(gam, i, d, K), gL = gam_at<PER_K>(gam, Lc - 1, d, K);
         cs = fmaf(aK[m], ks[i * K + d] * expf(gL - gi), cs);
       }
@@ -366,13 +435,6 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
     colsum[i_base * kKmax + d] = cs;
   }
   if (tid < K) gLs[tid] = gLacc;
-#pragma unroll
-  for (int m = 0; m < MP; ++m) {
-    const int r = m * PR + pr_base, i = pi;
-    float val = 0.f;
-    if (r < Lc && i <= r) val = PER_K ? aP[m] : aP[m] * expf(gam[r] - gam[i]);
-    dPs[r * C + i] = val;
-  }
   __syncthreads();
 
   if (d < K) {
@@ -765,8 +827,8 @@ int launch_bwd_dqkg(const BwdArgs &a) {
     constexpr int C = decltype(cfg)::C;
     constexpr bool PK = decltype(cfg)::PK;
     const int64_t K = f.d.K;
-    const size_t smem = sizeof(float) * (2 * C * K + (PK ? C * K : C) + 3 * kVt * (C + 1) + 2 * kVt * (K + 1) +
-                                         C * C + 2 * kKmax + K);
+    const size_t smem =
+        sizeof(float) * (2 * C * K + (PK ? C * K : C) + dqkg_region_floats(C, K) + C * C + 2 * kKmax + K);
     auto kern = bwd_dqkg_kernel<Tin, C, PK>;
     int rc = set_smem(kern, smem, "bwd_dqkg_kernel");
     if (rc != GDR_OK) return rc;
