@@ -38,7 +38,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBVd = 32;   // V-tile of the dh scan
-constexpr int kTw = 128;   // column tile of the triangular back substitution
 constexpr int kKmax = 128; // largest K of the backward
 
 struct ChunkPos {
@@ -481,13 +480,37 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
 }
 
 // --------------------------------------------------------------------------
-// wy: grid (nt_max, HV).  The UT transform's backward: back substitution with
-// (I + A)^T for dX (columns of dv_new) and dY (columns of dW), dA, then the
-// A-, w- and u-paths into dk^, dGamma, dbeta, dv; finally dg as the reverse
-// within-chunk cumsum of dGamma.
-// smem: ks[C*K] | gam[C*K or C] | bet[C] | Bm[C*C] | As[C*C] (A, then dB) |
-//       Xs[C*(kTw+1)] | Us[C*(kTw+1)] (then dGamma) | dbs[C] | rowacc[C]
+// wy: grid (nt_max, HV).  The UT transform's backward.  Bm = the decayed Gram
+// matrix of k (prep::decayed_gram, strict), A = diag(beta) Bm, T = (I + A)^-1
+// by blocks; then on tensor cores (3 x TF32) per 32-column tile
+//   dX = T^T dv_new  -> dv = diag(beta) dX, dbeta += rowsum(dX V), dA -= dX u^T
+//   dY = T^T dW      -> dA -= dY w^T
+// (dA accumulates in register fragments); then dbeta += rowsum(dA Bm) +
+// rowsum(dY K e^G), dB = beta_i dA, the k and Gamma terms of the Y and A paths
+// on CUDA cores, and dg as the reverse within-chunk cumsum of dGamma.
+// smem: ks[C][KL] | gam | bet, dbs, rowacc [C] | AT[C][C+1] (A / T, then dB) |
+//       Tm[C][C+4] | Bm[C][C+1] | sY[C][KL] | scratch (gram Xs, Ys; the V
+//       tiles; the dW tiles and w; the per-key dGamma)
 // --------------------------------------------------------------------------
+constexpr int kWt = 32;          // columns per tile
+constexpr int kLdB = kWt + 8;    // B operands read [k][n] (8 mod 32)
+constexpr int kLdA = kWt + 4;    // A operands / B read [n][k] (4 mod 32)
+
+__host__ __device__ constexpr int64_t wy_scratch_floats(int C, int64_t K, bool per_k) {
+  const int64_t KL = scan::kpad(K) + 4;
+  const int64_t a = prep::gram_scratch_floats(C, K, per_k);
+  const int64_t b = (int64_t)C * (kLdB + 2 * kLdA);
+  const int64_t c = (int64_t)C * (kLdB + KL);
+  const int64_t m = a > b ? a : b;
+  return (m > c ? m : c) > 1536 ? (m > c ? m : c) : 1536;
+}
+
+__host__ __device__ constexpr int64_t wy_smem_floats(int C, int64_t K, bool per_k) {
+  const int64_t KL = scan::kpad(K) + 4;
+  return C * KL + (per_k ? C * scan::kpad(K) : C) + 3 * C + C * (C + 1) + C * (C + 4) + C * (C + 1) + C * KL +
+         wy_scratch_floats(C, K, per_k);
+}
+
 template <typename Tin, int C, bool PER_K>
 __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
     const Tin *__restrict__ k, const Tin *__restrict__ v, const Tin *__restrict__ beta,
@@ -497,172 +520,180 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
     int beta_logits, float *__restrict__ dka, const float *__restrict__ dga, Tin *__restrict__ dv,
     Tin *__restrict__ dbeta, float *__restrict__ dg) {
   constexpr int MQ = C * kKmax / kThreads;
-  constexpr int MP = C * C / kThreads;
-  constexpr int PR = kThreads / C;
-  constexpr int LX = kTw + 1;
+  constexpr int LA = C + 1, LT = C + 4;
+  constexpr int MT = C / 16;
+  constexpr int NAW = MT * (C / 8) / 8;  // dA tiles per warp
   extern __shared__ float smem[];
+  const int64_t Kp = scan::kpad(K), KL = Kp + 4, GL = PER_K ? Kp : 1;
   float *ks = smem;
-  float *gam = ks + C * K;
-  float *bet = gam + (PER_K ? C * K : C);
-  float *Bm = bet + C;
-  float *As = Bm + C * C;
-  float *Xs = As + C * C;
-  float *Us = Xs + C * LX;
-  float *dbs = Us + C * LX;
+  float *gam = ks + C * KL;
+  float *bet = gam + (PER_K ? C * Kp : C);
+  float *dbs = bet + C;
   float *rowacc = dbs + C;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float *AT = rowacc + C;
+  float *Tm = AT + C * LA;
+  float *Bm = Tm + C * LT;
+  float *sY = Bm + C * LA;
+  float *scr = sY + C * KL;
+  float *Xs = scr, *Ys = scr + 16 * KL;                                     // gram
+  float *dvt = scr, *ut = scr + C * kLdB, *dxt = ut + C * kLdA;             // V tiles
+  float *dwt = scr, *wf = scr + C * kLdB;                                   // K tiles, w
+  float *gtot = scr;                                                         // per-key dGamma
+  float *dAs = AT;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, gq = lane >> 2, tq = lane & 3;
   const int64_t hv = blockIdx.y;
   ChunkPos cp;
   if (!chunk_pos(cu, chunk_indices, blockIdx.x, T, C, &cp)) return;
   const int64_t t0 = cp.t0;
   const int Lc = cp.Lc;
   const int64_t hq = hv / (HV / H);
+  const int64_t gw = PER_K ? K : 1;
   const int d = tid & (kKmax - 1), i_base = tid / kKmax;
-  const int pj = tid % C, pi_base = tid / C;
+  const int m0 = 16 * (warp % MT);
 
-  for (int i = warp; i < C; i += kWarps) load_row_normed(k, t0 + i, H, hq, K, i < Lc, l2, ks + i * K, lane);
-  load_gamma<PER_K>(gcum, t0, Lc, C, HV, hv, K, gam, tid);
+  prep::load_qk_rows<Tin, C>(nullptr, k, t0, Lc, H, hq, K, l2, nullptr, ks, KL);
+  for (int64_t e = tid; e < C * gw; e += kThreads) {
+    const int64_t i = e / gw, dd = e % gw;
+    gam[i * GL + dd] = i < Lc ? gcum[((t0 + i) * HV + hv) * gw + dd] : 0.f;
+  }
   for (int i = tid; i < C; i += kThreads) {
     bet[i] = i < Lc ? load_beta(beta, (t0 + i) * HV + hv, beta_logits) : 0.f;
     dbs[i] = 0.f;
     rowacc[i] = 0.f;
   }
   __syncthreads();
-  // Bm_ij = sum_d k_id k_jd exp(G_id - G_jd) (i > j), A = diag(beta) Bm
-  for (int p = warp; p < C * C; p += kWarps) {
-    const int i = p / C, j = p % C;
-    if (j >= i || i >= Lc) {
-      if (lane == 0) {
-        Bm[p] = 0.f;
-        As[p] = 0.f;
-      }
-      continue;
-    }
-    float s = 0.f;
-    for (int64_t dd = lane; dd < K; dd += 32) {
-      float t = ks[i * K + dd] * ks[j * K + dd];
-      if (PER_K) t *= expf(gam[i * K + dd] - gam[j * K + dd]);
-      s += t;
-    }
-    s = warp_sum(s);
-    if (lane == 0) {
-      const float b = s * (PER_K ? 1.f : expf(gam[i] - gam[j]));
-      Bm[p] = b;
-      As[p] = bet[i] * b;
-    }
-  }
-  __syncthreads();
-
-  float aA[MP];
-#pragma unroll
-  for (int m = 0; m < MP; ++m) aA[m] = 0.f;
-
-  // One tile of back substitution, x = (I + A)^-T rhs, in place in Xs with
-  // one column per thread; `rhs` is dv_new (ld = V) or dW (ld = K).  Rows at
-  // and past Lc stay zero (A has no entries there).
-  auto back_substitute = [&](const float *__restrict__ rhs, int64_t ld, int64_t col0, int64_t ncol,
-                             bool write_dv) {
-    if (tid < kTw) {
-      const int64_t col = col0 + tid;
-      const bool ok = col < ncol;
-      for (int i = 0; i < C; ++i) Xs[i * LX + tid] = (i < Lc && ok) ? rhs[((t0 + i) * HV + hv) * ld + col] : 0.f;
-      for (int i = Lc - 1; i >= 0; --i) {
-        float acc = Xs[i * LX + tid];
-        for (int j = i + 1; j < Lc; ++j) acc = fmaf(-As[j * C + i], Xs[j * LX + tid], acc);
-        Xs[i * LX + tid] = acc;
-        if (write_dv && ok) dv[((t0 + i) * HV + hv) * V + col] = from_f32<Tin>(bet[i] * acc);
-      }
-    }
-  };
-  // aA -= Xs Us^T over one tile of width nc
-  auto accumulate_dA = [&](int nc) {
-#pragma unroll
-    for (int m = 0; m < MP; ++m) {
-      const int i = m * PR + pi_base, j = pj;
-      if (i > j && i < Lc) {
-        float s = 0.f;
-        for (int c = 0; c < nc; ++c) s = fmaf(Xs[i * LX + c], Us[j * LX + c], s);
-        aA[m] -= s;
-      }
-    }
-  };
-
-  // u-path: dX, dv = diag(beta) dX, dbeta += rowsum(dX V), dA -= dX u^T
-  for (int64_t v0 = 0; v0 < V; v0 += kTw) {
-    back_substitute(dvn, V, v0, V, true);
-    for (int e = tid; e < C * kTw; e += kThreads) {
-      const int j = e / kTw, c = e % kTw;
-      Us[j * LX + c] = (j < Lc && v0 + c < V) ? u[((t0 + j) * HV + hv) * V + v0 + c] : 0.f;
-    }
-    __syncthreads();
-    accumulate_dA(kTw);
-    for (int i = warp; i < Lc; i += kWarps) {
-      float s = 0.f;
-      for (int c = lane; c < kTw; c += 32)
-        if (v0 + c < V) s = fmaf(Xs[i * LX + c], to_f32(v[((t0 + i) * HV + hv) * V + v0 + c]), s);
-      s = warp_sum(s);
-      if (lane == 0) dbs[i] += s;
-    }
-    __syncthreads();
-  }
-  // w-path: dY (kept in Xs), dA -= dY w^T
-  back_substitute(dW, K, 0, K, false);
-  for (int e = tid; e < C * kTw; e += kThreads) {
-    const int j = e / kTw, c = e % kTw;
-    Us[j * LX + c] = (j < Lc && c < K) ? w[((t0 + j) * HV + hv) * K + c] : 0.f;
-  }
-  __syncthreads();
-  accumulate_dA((int)K);
-  __syncthreads();
-
-  // dA staged; dbeta += rowsum(dA Bm); dB = beta_i dA (GDN folds its decay in)
-#pragma unroll
-  for (int m = 0; m < MP; ++m) {
-    const int i = m * PR + pi_base, j = pj;
-    As[i * C + j] = (i > j && i < Lc) ? aA[m] : 0.f;
-  }
-  __syncthreads();
-  for (int i = warp; i < Lc; i += kWarps) {
-    float s = 0.f;
-    for (int j = lane; j < i; j += 32) s = fmaf(As[i * C + j], Bm[i * C + j], s);
-    s = warp_sum(s);
-    if (lane == 0) dbs[i] += s;
-  }
-  __syncthreads();
+  // Bm_ij = sum_d k_id k_jd e^{G_id - G_jd} (i > j); A = diag(beta) Bm
+  prep::decayed_gram<C, PER_K, true>(ks, ks, KL, gam, GL, K, Lc, nullptr, Bm, LA, Xs, Ys);
   for (int e = tid; e < C * C; e += kThreads) {
     const int i = e / C, j = e % C;
-    if (i > j && i < Lc) As[e] *= bet[i] * (PER_K ? 1.f : expf(gam[i] - gam[j]));
+    if (j < i) AT[i * LA + j] = bet[i] * Bm[i * LA + j];
+  }
+  __syncthreads();
+  prep::solve_unit_lower<C>(AT, LA, scr);
+  for (int e = tid; e < C * C; e += kThreads) {
+    const int i = e / C, j = e % C;
+    Tm[i * LT + j] = prep::t_at(AT, LA, i, j);
+  }
+
+  float fA[NAW][4];
+#pragma unroll
+  for (int s2 = 0; s2 < NAW; ++s2)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) fA[s2][e] = 0.f;
+
+  // u-path: dX = T^T dv_new per tile; dv; dbeta += rowsum(dX V); acc += dX u^T
+  for (int64_t v0 = 0; v0 < V; v0 += kWt) {
+    __syncthreads();
+    for (int e = tid; e < C * kWt; e += kThreads) {
+      const int j = e / kWt, c = e % kWt;
+      const bool ok = j < Lc && v0 + c < V;
+      dvt[j * kLdB + c] = ok ? dvn[((t0 + j) * HV + hv) * V + v0 + c] : 0.f;
+      ut[j * kLdA + c] = ok ? u[((t0 + j) * HV + hv) * V + v0 + c] : 0.f;
+    }
+    __syncthreads();
+    for (int tix = warp; tix < MT * (kWt / 8); tix += kWarps) {
+      const int mm = 16 * (tix % MT), n0 = 8 * (tix / MT);
+      float dd4[4] = {0.f, 0.f, 0.f, 0.f};
+      prep::tile_acc<true, false>(dd4, Tm, LT, dvt, kLdB, mm, n0, C / 8);  // A(i, j) = T[j][i]
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = mm + gq + 8 * (e >> 1), c = n0 + 2 * tq + (e & 1);
+        dxt[i * kLdA + c] = dd4[e];
+        if (i < Lc && v0 + c < V) dv[((t0 + i) * HV + hv) * V + v0 + c] = from_f32<Tin>(bet[i] * dd4[e]);
+      }
+    }
+    __syncthreads();
+    for (int i = warp; i < Lc; i += kWarps) {
+      float sacc = 0.f;
+      const int64_t col = v0 + lane;
+      if (col < V) sacc = dxt[i * kLdA + lane] * to_f32(v[((t0 + i) * HV + hv) * V + col]);
+      sacc = warp_sum(sacc);
+      if (lane == 0) dbs[i] += sacc;
+    }
+#pragma unroll
+    for (int s2 = 0; s2 < NAW; ++s2) {
+      const int n0 = 8 * ((warp + 8 * s2) / MT);
+      prep::tile_acc<false, true>(fA[s2], dxt, kLdA, ut, kLdA, m0, n0, kWt / 8);  // B(v, j) = u[j][v]
+    }
+  }
+  // w-path: dY = T^T dW into sY, then acc += dY w^T
+  for (int64_t d0 = 0; d0 < Kp; d0 += kWt) {
+    __syncthreads();
+    for (int e = tid; e < C * kWt; e += kThreads) {
+      const int j = e / kWt, c = e % kWt;
+      dwt[j * kLdB + c] = (j < Lc && d0 + c < K) ? dW[((t0 + j) * HV + hv) * K + d0 + c] : 0.f;
+    }
+    __syncthreads();
+    for (int tix = warp; tix < MT * (kWt / 8); tix += kWarps) {
+      const int mm = 16 * (tix % MT), n0 = 8 * (tix / MT);
+      float dd4[4] = {0.f, 0.f, 0.f, 0.f};
+      prep::tile_acc<true, false>(dd4, Tm, LT, dwt, kLdB, mm, n0, C / 8);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = mm + gq + 8 * (e >> 1), c = n0 + 2 * tq + (e & 1);
+        if (d0 + c < Kp) sY[i * KL + d0 + c] = dd4[e];
+      }
+    }
+  }
+  __syncthreads();
+  for (int64_t e = tid; e < C * Kp; e += kThreads) {
+    const int j = (int)(e / Kp);
+    const int64_t dd = e % Kp;
+    wf[j * KL + dd] = (j < Lc && dd < K) ? w[((t0 + j) * HV + hv) * K + dd] : 0.f;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int s2 = 0; s2 < NAW; ++s2) {
+    const int n0 = 8 * ((warp + 8 * s2) / MT);
+    prep::tile_acc<false, true>(fA[s2], sY, KL, wf, KL, m0, n0, (int)(Kp / 8));
+  }
+  __syncthreads();  // AT (T) is dead: dA goes there
+#pragma unroll
+  for (int s2 = 0; s2 < NAW; ++s2) {
+    const int n0 = 8 * ((warp + 8 * s2) / MT);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = m0 + gq + 8 * (e >> 1), j = n0 + 2 * tq + (e & 1);
+      dAs[i * LA + j] = (j < i && i < Lc) ? -fA[s2][e] : 0.f;
+    }
+  }
+  __syncthreads();
+  // dbeta += rowsum(dA Bm) + rowsum(dY K e^G), one warp per row
+  for (int i = warp; i < Lc; i += kWarps) {
+    float sacc = 0.f;
+    for (int j = lane; j < i; j += 32) sacc = fmaf(dAs[i * LA + j], Bm[i * LA + j], sacc);
+    for (int64_t dd = lane; dd < K; dd += 32)
+      sacc = fmaf(sY[i * KL + dd], ks[i * KL + dd] * expf(PER_K ? gam[i * GL + dd] : gam[i]), sacc);
+    sacc = warp_sum(sacc);
+    if (lane == 0) dbs[i] += sacc;
+  }
+  __syncthreads();
+  // dB = beta_i dA (the scalar gate folds e^{G_i - G_j} in)
+  for (int e = tid; e < C * C; e += kThreads) {
+    const int i = e / C, j = e % C;
+    if (j < i && i < Lc) dAs[i * LA + j] *= bet[i] * (PER_K ? 1.f : expf(gam[i] - gam[j]));
   }
   __syncthreads();
 
-  // dbeta += rowsum(dY K e^G), one warp per row
-  for (int i = warp; i < Lc; i += kWarps) {
-    float s = 0.f;
-    for (int64_t dd = lane; dd < K; dd += 32)
-      s = fmaf(Xs[i * LX + dd], ks[i * K + dd] * expf(gam_at<PER_K>(gam, i, dd, K)), s);
-    s = warp_sum(s);
-    if (lane == 0) dbs[i] += s;
-  }
   // k^ and Gamma through Y = diag(beta) K e^G and through A
-  float *gtot = Us;
   if (d < K) {
 #pragma unroll 1
     for (int m = 0; m < MQ; ++m) {
       const int i = 2 * m + i_base;
       if (i >= Lc) continue;
-      const float gi = gam_at<PER_K>(gam, i, d, K);
-      const float eG = expf(gi), kv = ks[i * K + d], y = Xs[i * LX + d];
+      const float gi = PER_K ? gam[i * GL + d] : gam[i];
+      const float eG = expf(gi), kv = ks[i * KL + d], y = sY[i * KL + d];
       float dk = bet[i] * y * eG;
       float dgm = dk * kv;
       float t1 = 0.f, t2 = 0.f;
       for (int j = 0; j < i; ++j) {
-        float f = As[i * C + j] * ks[j * K + d];
-        if (PER_K) f *= expf(gi - gam[j * K + d]);
+        float f = dAs[i * LA + j] * ks[j * KL + d];
+        if (PER_K) f *= expf(gi - gam[j * GL + d]);
         t1 += f;
       }
       for (int r = i + 1; r < Lc; ++r) {
-        float f = As[r * C + i] * ks[r * K + d];
-        if (PER_K) f *= expf(gam[r * K + d] - gi);
+        float f = dAs[r * LA + i] * ks[r * KL + d];
+        if (PER_K) f *= expf(gam[r * GL + d] - gi);
         t2 += f;
       }
       dk += t1 + t2;
@@ -847,7 +878,7 @@ int launch_bwd_wy(const BwdArgs &a) {
     constexpr int C = decltype(cfg)::C;
     constexpr bool PK = decltype(cfg)::PK;
     const int64_t K = f.d.K;
-    const size_t smem = sizeof(float) * (C * K + (PK ? C * K : C) + C + 2 * C * C + 2 * C * (kTw + 1) + 2 * C);
+    const size_t smem = sizeof(float) * wy_smem_floats(C, K, PK);
     auto kern = bwd_wy_kernel<Tin, C, PK>;
     int rc = set_smem(kern, smem, "bwd_wy_kernel");
     if (rc != GDR_OK) return rc;
