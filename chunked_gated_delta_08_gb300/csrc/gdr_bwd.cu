@@ -258,15 +258,23 @@ __global__ void __launch_bounds__(kThreads) bwd_dh_kernel(
 // (3 x TF32, accumulators in registers), then forms the chunk's dq^, dk^ and
 // dGamma from the output and state terms on CUDA cores, where thread t owns
 // column d = t % 128 and rows i = 2m + t / 128 of every C x K matrix.
-// smem: qs[C*K] | ks[C*K] | gam[C*K or C] | tiles (do, dv_new, v_new [C][36],
-//       h, dh' [Kp][36]; then the staged dQt, dKb [C][Kp]; then the scalar
-//       gate's per-element dGamma) | dPs[C*C] | colsum[2*128] | gLs[K]
+// The sums over the other rows of the chunk (sq, sk) come from
+// prep::decayed_apply.
+// smem: qs, ks [C][Kp+8] | gam[C*K or C] | tiles (do, dv_new, v_new [C][36],
+//       h, dh' [Kp][36]; then the staged dQt, dKb [C][Kp]; then sq, sk;
+//       sq then the scalar gate's per-element dGamma) | dPs[C][C+4] |
+//       colsum[2*128] | gLs[K] | Xs, Ys (per-key gate)
 // --------------------------------------------------------------------------
 constexpr int kQL = 36;  // row stride of the V tiles (4 mod 32)
 
 __host__ __device__ constexpr int64_t dqkg_region_floats(int C, int64_t K) {
   return (3 * C + 2 * scan::kpad(K)) * kQL > 2 * C * scan::kpad(K) ? (3 * C + 2 * scan::kpad(K)) * kQL
                                                                      : 2 * C * scan::kpad(K);
+}
+
+__host__ __device__ constexpr int64_t dqkg_smem_floats(int C, int64_t K, bool per_k) {
+  return 2 * C * (scan::kpad(K) + 8) + (per_k ? C * K : C) + dqkg_region_floats(C, K) + C * (C + 4) + 2 * kKmax +
+         K + prep::gram_scratch_floats(C, K, per_k);
 }
 
 template <typename Tin, int C, bool PER_K>
@@ -281,18 +289,20 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
   constexpr int NTW = 16 * MT / 8;          // column tiles of a C x 128 product per warp
   constexpr int NPW = MT * (C / 8) / 8;     // tiles of dP per warp
   extern __shared__ float smem[];
-  const int64_t Kp = scan::kpad(K);
+  const int64_t Kp = scan::kpad(K), KQ = Kp + 8;
+  constexpr int LP = C + 4;
   float *qs = smem;
-  float *ks = qs + C * K;
-  float *gam = ks + C * K;
+  float *ks = qs + C * KQ;
+  float *gam = ks + C * KQ;
   float *reg = gam + (PER_K ? C * K : C);
   float *doA = reg, *dvA = doA + C * kQL, *vnA = dvA + C * kQL;
   float *hB = vnA + C * kQL, *dhB = hB + Kp * kQL;
   float *sQ = reg, *sK = reg + C * Kp;  // after the V loop
-  float *rowbuf = reg;                  // after sQ, sK are read
+  float *lo = reg, *up = reg + C * Kp;  // after sQ, sK are read; lo then the scalar gate's dGamma
   float *dPs = reg + dqkg_region_floats(C, K);
-  float *colsum = dPs + C * C;
+  float *colsum = dPs + C * LP;
   float *gLs = colsum + 2 * kKmax;
+  float *Xs = gLs + K, *Ys = Xs + 16 * KQ;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, gq = lane >> 2, tq = lane & 3;
   const int64_t chunk = blockIdx.x, hv = blockIdx.y;
   ChunkPos cp;
@@ -304,14 +314,11 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
   const int ntk = (int)(Kp / 8);  // column tiles of a C x Kp product
   const int m0 = 16 * (warp % MT);
 
-  for (int i = warp; i < C; i += kWarps) {
-    load_row_normed(q, t0 + i, H, hq, K, i < Lc, l2, qs + i * K, lane);
-    load_row_normed(k, t0 + i, H, hq, K, i < Lc, l2, ks + i * K, lane);
-  }
+  prep::load_qk_rows<Tin, C>(q, k, t0, Lc, H, hq, K, l2, qs, ks, KQ);
   load_gamma<PER_K>(gcum, t0, Lc, C, HV, hv, K, gam, tid);
   for (int e = tid; e < 2 * kKmax; e += kThreads) colsum[e] = 0.f;
 
-  float aQ[MQ], aW[MQ], aK[MQ];
+  float aQ[MQ], aK[MQ];
   float fQ[NTW][4], fW[NTW][4], fK[NTW][4], fP[NPW][4];
 #pragma unroll
   for (int s = 0; s < NTW; ++s)
@@ -406,7 +413,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
       const int r = m0 + gq + 8 * (e >> 1), i = n0 + 2 * tq + (e & 1);
       float val = 0.f;
       if (r < Lc && i <= r) val = PER_K ? fP[s][e] : fP[s][e] * expf(gam[r] - gam[i]);
-      dPs[r * C + i] = val;
+      dPs[r * LP + i] = val;
     }
   }
   __syncthreads();
@@ -415,9 +422,10 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
     const int i = 2 * m + i_base;
     aQ[m] = d < K ? sQ[i * Kp + d] : 0.f;
     aK[m] = d < K ? sK[i * Kp + d] : 0.f;
-    aW[m] = 0.f;
   }
-  __syncthreads();  // rowbuf may now reuse the staging
+  __syncthreads();  // the staging is dead
+  // sq = sum_{j <= i} dP_ij k_j e^{G_i - G_j} (lo), sk = sum_{r >= i} dP_ri q_r e^{G_r - G_i} (up)
+  prep::decayed_apply<C, PER_K, false>(dPs, LP, ks, qs, KQ, gam, PER_K ? K : 1, K, Lc, lo, up, Kp, Xs, Ys);
 
   // dW out; dP staged (GDN folds its decay in); column sums of dKb * Kb,
   // each thread's half in a fixed slot so the sum's order is fixed
@@ -428,7 +436,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
       const int i = 2 * m + i_base;
       if (i < Lc) {
         const float gi = gam_at<PER_K>(gam, i, d, K), gL = gam_at<PER_K>(gam, Lc - 1, d, K);
-        cs = fmaf(aK[m], ks[i * K + d] * expf(gL - gi), cs);
+        cs = fmaf(aK[m], ks[i * KQ + d] * expf(gL - gi), cs);
       }
     }
     colsum[i_base * kKmax + d] = cs;
@@ -443,20 +451,10 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
       if (i >= Lc) continue;
       const float gi = gam_at<PER_K>(gam, i, d, K), gL = gam_at<PER_K>(gam, Lc - 1, d, K);
       const float eG = expf(gi), eL = expf(gL - gi);
-      const float qv = qs[i * K + d], kv = ks[i * K + d];
+      const float qv = qs[i * KQ + d], kv = ks[i * KQ + d];
       float dq = aQ[m] * eG, dk = aK[m] * eL;
       float dgm = aQ[m] * qv * eG - aK[m] * kv * eL;
-      float sq = 0.f, sk = 0.f;
-      for (int j = 0; j <= i; ++j) {
-        float f = dPs[i * C + j] * ks[j * K + d];
-        if (PER_K) f *= expf(gi - gam[j * K + d]);
-        sq += f;
-      }
-      for (int r = i; r < Lc; ++r) {
-        float f = dPs[r * C + i] * qs[r * K + d];
-        if (PER_K) f *= expf(gam[r * K + d] - gi);
-        sk += f;
-      }
+      const float sq = lo[i * Kp + d], sk = up[i * Kp + d];
       dq += sq;
       dk += sk;
       dgm += qv * sq - kv * sk;
@@ -465,14 +463,14 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
       dqa[row * K + d] = dq;
       dka[row * K + d] = dk;
       if (PER_K) dga[row * K + d] = dgm;
-      else rowbuf[i * K + d] = dgm;
+      else lo[i * Kp + d] = dgm;  // this thread's own entry: read above
     }
   }
   if (!PER_K) {  // scalar gate: dGamma_i = sum_d, one warp per row
     __syncthreads();
     for (int i = warp; i < Lc; i += kWarps) {
       float acc = 0.f;
-      for (int64_t dd = lane; dd < K; dd += 32) acc += rowbuf[i * K + dd];
+      for (int64_t dd = lane; dd < K; dd += 32) acc += lo[i * Kp + dd];
       acc = warp_sum(acc);
       if (lane == 0) dga[(t0 + i) * HV + hv] = acc;
     }
@@ -507,7 +505,7 @@ __host__ __device__ constexpr int64_t wy_scratch_floats(int C, int64_t K, bool p
 
 __host__ __device__ constexpr int64_t wy_smem_floats(int C, int64_t K, bool per_k) {
   const int64_t KL = scan::kpad(K) + 4;
-  return C * KL + (per_k ? C * scan::kpad(K) : C) + 3 * C + C * (C + 1) + C * (C + 4) + C * (C + 1) + C * KL +
+  return C * KL + (per_k ? C * scan::kpad(K) : C) + 3 * C + C * (C + 1) + C * (C + 4) + C * (C + 1) + 2 * C * KL +
          wy_scratch_floats(C, K, per_k);
 }
 
@@ -534,11 +532,12 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
   float *Tm = AT + C * LA;
   float *Bm = Tm + C * LT;
   float *sY = Bm + C * LA;
-  float *scr = sY + C * KL;
+  float *up = sY + C * KL;  // then the per-element dGamma
+  float *scr = up + C * KL;
   float *Xs = scr, *Ys = scr + 16 * KL;                                     // gram
   float *dvt = scr, *ut = scr + C * kLdB, *dxt = ut + C * kLdA;             // V tiles
   float *dwt = scr, *wf = scr + C * kLdB;                                   // K tiles, w
-  float *gtot = scr;                                                         // per-key dGamma
+  float *gtot = up;
   float *dAs = AT;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, gq = lane >> 2, tq = lane & 3;
   const int64_t hv = blockIdx.y;
@@ -675,39 +674,36 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
   }
   __syncthreads();
 
-  // k^ and Gamma through Y = diag(beta) K e^G and through A
+  // k^ and Gamma through Y = diag(beta) K e^G and through A:
+  // t1 = sum_{j < i} dB_ij k_j e^{G_i - G_j} (lo, over sY), t2 = sum_{r > i} dB_ri k_r e^{G_r - G_i} (up)
+  float yv[MQ];
+#pragma unroll
+  for (int m = 0; m < MQ; ++m) yv[m] = d < K ? sY[(2 * m + i_base) * KL + d] : 0.f;
+  __syncthreads();
+  float *lo = sY;
+  prep::decayed_apply<C, PER_K, true>(dAs, LA, ks, ks, KL, gam, GL, K, Lc, lo, up, KL, scr, scr + 16 * KL);
   if (d < K) {
-#pragma unroll 1
+#pragma unroll
     for (int m = 0; m < MQ; ++m) {
       const int i = 2 * m + i_base;
       if (i >= Lc) continue;
       const float gi = PER_K ? gam[i * GL + d] : gam[i];
-      const float eG = expf(gi), kv = ks[i * KL + d], y = sY[i * KL + d];
+      const float eG = expf(gi), kv = ks[i * KL + d], y = yv[m];
       float dk = bet[i] * y * eG;
       float dgm = dk * kv;
-      float t1 = 0.f, t2 = 0.f;
-      for (int j = 0; j < i; ++j) {
-        float f = dAs[i * LA + j] * ks[j * KL + d];
-        if (PER_K) f *= expf(gi - gam[j * GL + d]);
-        t1 += f;
-      }
-      for (int r = i + 1; r < Lc; ++r) {
-        float f = dAs[r * LA + i] * ks[r * KL + d];
-        if (PER_K) f *= expf(gam[r * GL + d] - gi);
-        t2 += f;
-      }
+      const float t1 = lo[i * KL + d], t2 = up[i * KL + d];
       dk += t1 + t2;
       dgm += kv * (t1 - t2);
       const int64_t row = (t0 + i) * HV + hv;
       dka[row * K + d] += dk;
-      gtot[i * K + d] = PER_K ? dga[row * K + d] + dgm : dgm;
+      gtot[i * KL + d] = PER_K ? dga[row * K + d] + dgm : dgm;  // this thread's own entry of up
     }
   }
   __syncthreads();
   if (!PER_K) {  // scalar gate: dGamma_i = sum_d, one warp per row
     for (int i = warp; i < Lc; i += kWarps) {
       float acc = 0.f;
-      for (int64_t dd = lane; dd < K; dd += 32) acc += gtot[i * K + dd];
+      for (int64_t dd = lane; dd < K; dd += 32) acc += gtot[i * KL + dd];
       acc = warp_sum(acc);
       if (lane == 0) rowacc[i] = acc;
     }
@@ -719,7 +715,7 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
     for (int64_t dd = tid; dd < K; dd += kThreads) {
       float run = 0.f;
       for (int i = Lc - 1; i >= 0; --i) {
-        run += gtot[i * K + dd];
+        run += gtot[i * KL + dd];
         dg[((t0 + i) * HV + hv) * K + dd] = run;
       }
     }
@@ -858,8 +854,7 @@ int launch_bwd_dqkg(const BwdArgs &a) {
     constexpr int C = decltype(cfg)::C;
     constexpr bool PK = decltype(cfg)::PK;
     const int64_t K = f.d.K;
-    const size_t smem =
-        sizeof(float) * (2 * C * K + (PK ? C * K : C) + dqkg_region_floats(C, K) + C * C + 2 * kKmax + K);
+    const size_t smem = sizeof(float) * dqkg_smem_floats(C, K, PK);
     auto kern = bwd_dqkg_kernel<Tin, C, PK>;
     int rc = set_smem(kern, smem, "bwd_dqkg_kernel");
     if (rc != GDR_OK) return rc;

@@ -237,9 +237,10 @@ __device__ __forceinline__ void load_qk_rows(const Tin *__restrict__ q, const Ti
 // directly instead.
 __host__ __device__ constexpr bool gram_factored(int64_t K) { return K <= 128; }
 
-// Floats of scratch (Xs, Ys) decayed_gram needs for K (row stride kpad(K)+4).
+// Floats of scratch (Xs, Ys: 16 + 48 rows at C = 64) decayed_gram and
+// decayed_apply need, for row strides up to kpad(K) + 8.
 __host__ __device__ constexpr int64_t gram_scratch_floats(int C, int64_t K, bool per_k) {
-  return per_k && gram_factored(K) ? (16 + C) * (scan::kpad(K) + 4) : 0;
+  return per_k && gram_factored(K) ? C * (scan::kpad(K) + 8) : 0;
 }
 
 // out[i][j] = s_i sum_d X_id Y_jd e^{G_id - G_jd} for j < i (STRICT) or
@@ -281,6 +282,11 @@ __device__ void decayed_gram(const float *X, const float *Y, int64_t xl, const f
   }
   const bool factored = gram_factored(K);
   const int per_row = factored ? 16 : C;
+  if (factored)  // block rows starting past Lc are skipped below: their entries are zero
+    for (int e = tid; e < C * C; e += 256) {
+      const int i = e / C, j = e % C;
+      if (i >= Lc && j < 16 * (i / 16)) out[i * lo + j] = 0.f;
+    }
   for (int p = warp; p < C * per_row; p += kWarps) {
     const int i = p / per_row, j = (factored ? 16 * (i / 16) : 0) + p % per_row;
     if (!below(i, j) || i >= Lc) {
@@ -293,7 +299,7 @@ __device__ void decayed_gram(const float *X, const float *Y, int64_t xl, const f
     acc = warp_sum(acc);
     if (lane == 0) out[i * lo + j] = (s ? s[i] : 1.f) * acc;
   }
-  for (int a = 1; factored && a < C / 16; ++a) {
+  for (int a = 1; factored && a < C / 16 && 16 * a < Lc; ++a) {
     const int r = 16 * a;
     __syncthreads();
     for (int64_t e = tid; e < (16 + r) * Kp; e += 256) {
@@ -301,7 +307,7 @@ __device__ void decayed_gram(const float *X, const float *Y, int64_t xl, const f
       const int64_t d = e % Kp;
       if (row < 16) {
         const int i = r + row;
-        Xs[row * xl + d] = d < K ? X[i * xl + d] * expf(gam[i * gl + d] - gam[r * gl + d]) : 0.f;
+        Xs[row * xl + d] = (d < K && i < Lc) ? X[i * xl + d] * expf(gam[i * gl + d] - gam[r * gl + d]) : 0.f;
       } else {
         const int jr = row - 16;
         Ys[jr * xl + d] = d < K ? Y[jr * xl + d] * expf(gam[r * gl + d] - gam[jr * gl + d]) : 0.f;
@@ -319,6 +325,122 @@ __device__ void decayed_gram(const float *X, const float *Y, int64_t xl, const f
     }
   }
   __syncthreads();
+}
+
+// Both sides of a decayed product with a lower-triangular C x C matrix M
+// (row stride lm; zero above the diagonal, and on it when STRICT):
+//   lo[i][d] = sum_{j < i (<= i)} M[i][j] Ylo[j][d] e^{G_id - G_jd}
+//   up[i][d] = sum_{r > i (>= i)} M[r][i] Yup[r][d] e^{G_rd - G_id}
+// for i < Lc, d < kpad(K) (outputs with row stride lw; zero past K; rows past
+// Lc are zero or unspecified).  M, Y rows past Lc must be zero; no row past Lc
+// enters a decay factor (their G is a placeholder).  Y rows have stride yl
+// (zero past K).  Scalar gate: the decay must
+// already be folded into M, and lo = M Y, up = M^T Y are plain products.
+// Per-key gate: diagonal 16 x 16 blocks term by term; for block row a > 0
+// (r0 = 16 a) the block products
+//   lo[i] += e^{G_i - G_r0} (M[i, :r0] (Y_j e^{G_r0 - G_j}))        i in block a
+//   up[i] += e^{G_r0 - G_i} (M[block a, i]^T (Y_r e^{G_r - G_r0}))  i < r0
+// where every exponent is non-positive for non-positive gates.  Xs, Ys:
+// scratch of gram_scratch_floats.  All 256 threads; ends with a barrier.
+template <int C, bool PER_K, bool STRICT>
+__device__ void decayed_apply(const float *M, int lm, const float *Ylo, const float *Yup, int64_t yl, const float *gam,
+                              int64_t gl, int64_t K, int Lc, float *lo, float *up, int64_t lw, float *Xs, float *Ys) {
+  constexpr int kWarps = 8;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, gq = lane >> 2, tq = lane & 3;
+  const int64_t Kp = scan::kpad(K);
+  const int nkt = (int)(Kp / 8);
+  if constexpr (!PER_K) {
+    {
+      for (int tix = warp; tix < (C / 16) * nkt; tix += kWarps) {
+        const int m0 = 16 * (tix % (C / 16)), n0 = 8 * (tix / (C / 16));
+        float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_acc<false, false>(a, M, lm, Ylo, yl, m0, n0, C / 8);
+        tile_acc<true, false>(b, M, lm, Yup, yl, m0, n0, C / 8);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = m0 + gq + 8 * (e >> 1), d = n0 + 2 * tq + (e & 1);
+          lo[i * lw + d] = a[e];
+          up[i * lw + d] = b[e];
+        }
+      }
+    }
+    __syncthreads();
+  } else {
+  if (!gram_factored(K)) {  // per-key gate past K = 128: every term directly
+    {
+      for (int64_t e = tid; e < C * Kp; e += 256) {
+        const int i = (int)(e / Kp);
+        const int64_t d = e % Kp;
+        float a = 0.f, b = 0.f;
+        if (d < K && i < Lc) {
+          const float gi = gam[i * gl + d];
+          for (int j = 0; j < Lc; ++j) {
+            if (STRICT ? j < i : j <= i) a = fmaf(M[i * lm + j] * Ylo[j * yl + d], expf(gi - gam[j * gl + d]), a);
+            if (STRICT ? j > i : j >= i) b = fmaf(M[j * lm + i] * Yup[j * yl + d], expf(gam[j * gl + d] - gi), b);
+          }
+        }
+        lo[i * lw + d] = a;
+        up[i * lw + d] = b;
+      }
+    }
+    __syncthreads();
+    return;
+  }
+  // diagonal blocks, term by term
+  for (int64_t e = tid; e < C * Kp; e += 256) {
+    const int i = (int)(e / Kp);
+    const int64_t d = e % Kp;
+    float a = 0.f, b = 0.f;
+    if (d < K && i < Lc) {
+      const int base = 16 * (i / 16), end = base + 16 < Lc ? base + 16 : Lc;
+      const float gi = gam[i * gl + d];
+      for (int j = base; j < end; ++j) {
+        if (STRICT ? j < i : j <= i) a = fmaf(M[i * lm + j] * Ylo[j * yl + d], expf(gi - gam[j * gl + d]), a);
+        if (STRICT ? j > i : j >= i) b = fmaf(M[j * lm + i] * Yup[j * yl + d], expf(gam[j * gl + d] - gi), b);
+      }
+    }
+    lo[i * lw + d] = a;
+    up[i * lw + d] = b;
+  }
+  for (int a = 1; a < C / 16 && 16 * a < Lc; ++a) {
+    const int r0 = 16 * a;
+    __syncthreads();
+    for (int64_t e = tid; e < (16 + r0) * Kp; e += 256) {
+      const int row = (int)(e / Kp);
+      const int64_t d = e % Kp;
+      if (row < 16) {  // Y_r e^{G_r - G_r0}, r in block a (zero past Lc)
+        const int r = r0 + row;
+        Xs[row * yl + d] = (d < K && r < Lc) ? Yup[r * yl + d] * expf(gam[r * gl + d] - gam[r0 * gl + d]) : 0.f;
+      } else {  // Y_j e^{G_r0 - G_j}, j < r0
+        const int j = row - 16;
+        Ys[j * yl + d] = d < K ? Ylo[j * yl + d] * expf(gam[r0 * gl + d] - gam[j * gl + d]) : 0.f;
+      }
+    }
+    __syncthreads();
+    // lo rows r0 .. r0+15: M[r0.., :r0] Ys, scaled by e^{G_i - G_r0}
+    for (int nt = warp; nt < nkt; nt += kWarps) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      tile_acc<false, false>(acc, M + r0 * lm, lm, Ys, yl, 0, 8 * nt, r0 / 8);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = r0 + gq + 8 * (e >> 1), d = 8 * nt + 2 * tq + (e & 1);
+        if (d < K && i < Lc) lo[i * lw + d] += acc[e] * expf(gam[i * gl + d] - gam[r0 * gl + d]);
+      }
+    }
+    // up rows 0 .. r0-1: M[block a, :r0]^T Xs, scaled by e^{G_r0 - G_i}
+    for (int tix = warp; tix < (r0 / 16) * nkt; tix += kWarps) {
+      const int m0 = 16 * (tix % (r0 / 16)), n0 = 8 * (tix / (r0 / 16));
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      tile_acc<true, false>(acc, M + r0 * lm, lm, Xs, yl, m0, n0, 2);  // A(i, r) = M[r0 + r][i]
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = m0 + gq + 8 * (e >> 1), d = n0 + 2 * tq + (e & 1);
+        if (d < K && i < Lc) up[i * lw + d] += acc[e] * expf(gam[r0 * gl + d] - gam[i * gl + d]);
+      }
+    }
+  }
+  __syncthreads();
+  }
 }
 
 }  // namespace prep
