@@ -219,41 +219,90 @@ def bwd(q, k, v, g, beta, do, dht=None, h0=None, cu_seqlens=None, chunk_size=64,
 
 def fwd_host(q, k, v, g, beta, h0=None, cu_seqlens=None, chunk_size=64, use_qk_l2norm=False,
              output_final_state=True, algo="auto", device="cuda", out_host=None, final_state_host=None,
-             dev_buffers=None, stream=None):
+             dev_buffers=None, stream=None, pieces=4, beta_logits=False):
     """End-to-end call on HOST tensors: copy inputs in, run, copy o (and ht) back.
 
     Host tensors should be pinned for asynchronous copies.  ``dev_buffers`` may
-    hold reusable device tensors (a dict keyed by input name, plus ``o``, ``ht``);
-    the copies are enqueued on ``stream`` and the call returns after the
-    device-to-host copies complete.
+    hold reusable device tensors (a dict keyed by input name, plus ``o``, ``ht``
+    and the side streams); the call returns after the device-to-host copies
+    complete.  A dense batch (no cu_seqlens, B > 1) is processed in up to
+    ``pieces`` slices of whole sequences, pipelined on three streams: the
+    host-to-device copy of slice p+1, the forward of slice p and the
+    device-to-host copy of slice p-1 overlap.  Sequences are independent, so
+    the results are those of one call on the whole batch.
     """
     s = stream if stream is not None else torch.cuda.current_stream()
     bufs = dev_buffers if dev_buffers is not None else {}
+    B = q.shape[0]
+    inputs = (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("h0", h0), ("cu_seqlens", cu_seqlens))
     dev = {}
-    with torch.cuda.stream(s):
-        for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("h0", h0),
-                        ("cu_seqlens", cu_seqlens)):
-            if t is None:
-                dev[name] = None
-                continue
-            d = bufs.get(name)
-            if d is None or d.shape != t.shape or d.dtype != t.dtype:
-                d = torch.empty(t.shape, dtype=t.dtype, device=device)
-                bufs[name] = d
-            d.copy_(t, non_blocking=True)
-            dev[name] = d
-        o, ht = fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], h0=dev["h0"],
-                    cu_seqlens=dev["cu_seqlens"], chunk_size=chunk_size, use_qk_l2norm=use_qk_l2norm,
-                    output_final_state=output_final_state, algo=algo, out=bufs.get("o"),
-                    final_state=bufs.get("ht"), stream=s)
-        bufs["o"], bufs["ht"] = o, ht
-        o_h = out_host if out_host is not None else torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-        o_h.copy_(o, non_blocking=True)
-        ht_h = None
-        if ht is not None:
-            ht_h = final_state_host if final_state_host is not None else torch.empty(ht.shape, dtype=ht.dtype,
-                                                                                    pin_memory=True)
-            ht_h.copy_(ht, non_blocking=True)
+    for name, t in inputs:
+        if t is None:
+            dev[name] = None
+            continue
+        d = bufs.get(name)
+        if d is None or d.shape != t.shape or d.dtype != t.dtype:
+            d = torch.empty(t.shape, dtype=t.dtype, device=device)
+            bufs[name] = d
+        dev[name] = d
+    HV, V, K = v.shape[2], v.shape[3], q.shape[3]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    o = bufs.get("o")
+    if o is None or o.shape != v.shape or o.dtype != q.dtype:
+        o = torch.empty(v.shape, dtype=q.dtype, device=device)
+        bufs["o"] = o
+    ht = None
+    if output_final_state:
+        ht = bufs.get("ht")
+        if ht is None or ht.shape != (N, HV, K, V):
+            ht = torch.empty(N, HV, K, V, dtype=torch.float32, device=device)
+            bufs["ht"] = ht
+    o_h = out_host if out_host is not None else torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    ht_h = None
+    if ht is not None:
+        ht_h = final_state_host if final_state_host is not None else torch.empty(ht.shape, dtype=ht.dtype,
+                                                                                pin_memory=True)
+    P = max(1, min(int(pieces), B)) if cu_seqlens is None else 1
+    if P == 1:
+        with torch.cuda.stream(s):
+            for name, t in inputs:
+                if t is not None:
+                    dev[name].copy_(t, non_blocking=True)
+            fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], h0=dev["h0"], cu_seqlens=dev["cu_seqlens"],
+                chunk_size=chunk_size, use_qk_l2norm=use_qk_l2norm, output_final_state=output_final_state,
+                algo=algo, out=o, final_state=ht, stream=s, beta_logits=beta_logits)
+            o_h.copy_(o, non_blocking=True)
+            if ht is not None:
+                ht_h.copy_(ht, non_blocking=True)
+        s.synchronize()
+        return o_h, ht_h
+    s_in = bufs.setdefault("_stream_in", torch.cuda.Stream(device=device))
+    s_out = bufs.setdefault("_stream_out", torch.cuda.Stream(device=device))
+    s_in.wait_stream(s)
+    bounds = [B * p // P for p in range(P + 1)]
+    done = []
+    for p in range(P):
+        b0, b1 = bounds[p], bounds[p + 1]
+        with torch.cuda.stream(s_in):
+            for name, t in inputs:
+                if t is not None:
+                    dev[name][b0:b1].copy_(t[b0:b1], non_blocking=True)
+            ev_in = torch.cuda.Event()
+            ev_in.record(s_in)
+        s.wait_event(ev_in)
+        fwd(dev["q"][b0:b1], dev["k"][b0:b1], dev["v"][b0:b1], dev["g"][b0:b1], dev["beta"][b0:b1],
+            h0=None if dev["h0"] is None else dev["h0"][b0:b1], chunk_size=chunk_size, use_qk_l2norm=use_qk_l2norm,
+            output_final_state=output_final_state, algo=algo, out=o[b0:b1],
+            final_state=None if ht is None else ht[b0:b1], stream=s, beta_logits=beta_logits)
+        ev_c = torch.cuda.Event()
+        ev_c.record(s)
+        s_out.wait_event(ev_c)
+        with torch.cuda.stream(s_out):
+            o_h[b0:b1].copy_(o[b0:b1], non_blocking=True)
+            if ht is not None:
+                ht_h[b0:b1].copy_(ht[b0:b1], non_blocking=True)
+        done.append(ev_c)
+    s_out.synchronize()
     s.synchronize()
     return o_h, ht_h
 

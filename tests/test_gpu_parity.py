@@ -260,6 +260,19 @@ def test_host_buffers_end_to_end(gdr):
     assert not o_h.is_cuda and torch.equal(o_h, o_d.cpu()) and torch.equal(ht_h, ht_d.cpu())
 
 
+@pytest.mark.parametrize("algo", ["auto", "chunked"])
+def test_host_buffers_pipelined_dense(gdr, algo):
+    """A dense batch goes through fwd_host in pipelined slices; results equal one device call bit for bit."""
+    w, x = wl.random_case(5, 300, 2, 4, 128, 128, dtype=torch.bfloat16, seed=61)
+    pinned = {k: (None if v is None else v.pin_memory()) for k, v in x.items()}
+    bufs = {}
+    for _ in range(2):  # the second call reuses the device buffers and side streams
+        o_h, ht_h = gdr.fwd_host(pinned["q"], pinned["k"], pinned["v"], pinned["g"], pinned["beta"],
+                                 h0=pinned["h0"], use_qk_l2norm=True, algo=algo, dev_buffers=bufs, pieces=3)
+    o_d, ht_d = run_gpu(gdr, x, 64, True, algo, poison=False)
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(ht_h, ht_d.cpu())
+
+
 # ---------------------------------------------------------------- fused tensor-core form
 FUSED_GRID = [
     # B, T, H, HV, lengths
