@@ -280,7 +280,6 @@ def fwd_host(q, k, v, g, beta, h0=None, cu_seqlens=None, chunk_size=64, use_qk_l
     s_out = bufs.setdefault("_stream_out", torch.cuda.Stream(device=device))
     s_in.wait_stream(s)
     bounds = [B * p // P for p in range(P + 1)]
-    done = []
     for p in range(P):
         b0, b1 = bounds[p], bounds[p + 1]
         with torch.cuda.stream(s_in):
@@ -301,7 +300,6 @@ def fwd_host(q, k, v, g, beta, h0=None, cu_seqlens=None, chunk_size=64, use_qk_l
             o_h[b0:b1].copy_(o[b0:b1], non_blocking=True)
             if ht is not None:
                 ht_h[b0:b1].copy_(ht[b0:b1], non_blocking=True)
-        done.append(ev_c)
     s_out.synchronize()
     s.synchronize()
     return o_h, ht_h

@@ -48,28 +48,6 @@ __device__ __forceinline__ bool chunk_coords(const int64_t *chunk_indices, int64
   return true;
 }
 
-// Loads one token row of q or k (head hq) into smem, L2-normalized if asked.
-// Called by a whole warp; rows past the chunk's end are zero.
-template <typename Tin>
-__device__ __forceinline__ void load_row_normed(const Tin *__restrict__ x, int64_t tok, int64_t H, int64_t hq,
-                                                int64_t K, bool valid, bool l2, float *dst, int lane) {
-  float r[8];
-  float ss = 0.f;
-#pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    const int64_t d = lane + 32 * m;
-    r[m] = (valid && d < K) ? to_f32(x[(tok * H + hq) * K + d]) : 0.f;
-    ss += r[m] * r[m];
-  }
-  float scale = 1.f;
-  if (l2) scale = rsqrtf(warp_sum(ss) + kL2Eps);
-#pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    const int64_t d = lane + 32 * m;
-    if (d < K) dst[d] = r[m] * scale;
-  }
-}
-
 // beta as stored, or the logistic sigmoid of a stored logit (the "raw beta"
 // input of the coverage guide, section 三).
 template <typename Tin>
