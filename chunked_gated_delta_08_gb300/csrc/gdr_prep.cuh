@@ -287,17 +287,16 @@ __device__ void decayed_gram(const float *X, const float *Y, int64_t xl, const f
       const int i = e / C, j = e % C;
       if (i >= Lc && j < 16 * (i / 16)) out[i * lo + j] = 0.f;
     }
-  for (int p = warp; p < C * per_row; p += kWarps) {
+  // one thread per entry: a plain loop over d, no cross-lane reduction
+  for (int p = tid; p < C * per_row; p += 256) {
     const int i = p / per_row, j = (factored ? 16 * (i / 16) : 0) + p % per_row;
-    if (!below(i, j) || i >= Lc) {
-      if (lane == 0) out[i * lo + j] = 0.f;
-      continue;
-    }
     float acc = 0.f;
-    for (int64_t d = lane; d < K; d += 32)
-      acc = fmaf(X[i * xl + d] * Y[j * xl + d], expf(gam[i * gl + d] - gam[j * gl + d]), acc);
-    acc = warp_sum(acc);
-    if (lane == 0) out[i * lo + j] = (s ? s[i] : 1.f) * acc;
+    if (below(i, j) && i < Lc) {
+      const float *xr = X + i * xl, *yr = Y + j * xl, *gi = gam + i * gl, *gj = gam + j * gl;
+      for (int64_t d = 0; d < K; ++d) acc = fmaf(xr[d] * yr[d], expf(gi[d] - gj[d]), acc);
+      acc *= s ? s[i] : 1.f;
+    }
+    out[i * lo + j] = acc;
   }
   for (int a = 1; factored && a < C / 16 && 16 * a < Lc; ++a) {
     const int r = 16 * a;
