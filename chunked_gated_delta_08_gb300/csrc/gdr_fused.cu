@@ -24,12 +24,14 @@
 // they land.
 //
 // Warp roles (512 threads):
-//   warps 0-3   chain: the state recurrence of chunk c -- the v_new epilogue,
-//               the decay of the fp32 state held in TMEM (the next MMA adds
-//               dH into it), and the bf16 copy of the new state;
+//   warps 0-3   chain: the state recurrence of chunk c -- the w and v_new
+//               epilogues, the decay of the fp32 state held in TMEM (the next
+//               MMA adds dH into it), the bf16 copy of the new state -- and
+//               the output epilogue of chunk c (staged in the v_new tile,
+//               written by two TMA tensor stores);
 //   warps 4-11  prep: everything of chunk c that does not need the state
-//               (norms, gate cumsum, A, the solve, W', U', w, P) plus the
-//               output epilogue of chunk c-1;
+//               (norms, gate cumsum, A, the solve, W', U', P), so it can
+//               start chunk c+1 while the tensor cores turn W', U' into w, u;
 //   warp 12     producer: TMA loads of q, k (3-slot ring) and v (1 slot), g, beta;
 //   warp 13     MMA issuer: one thread issues every tcgen05.mma in a fixed order.
 // Hand-offs are mbarriers, each completing once per chunk.  Every wait is
@@ -98,7 +100,7 @@ struct Small {
   float gL[4];                  // chain: G at the chunk's last valid row
   float X[32 * 32];             // solve scratch
   uint64_t full_qk[kQKSlots], empty_qk[kQKSlots], full_v, empty_v;
-  uint64_t b_s, b_sfree, b_prep, b_w, b_wepi, b_pend, b_vn, b_vnepi, b_h, b_state, b_final;
+  uint64_t b_s, b_sfree, b_prep, b_w, b_wepi, b_pend, b_vn, b_vnepi, b_h, b_state, b_oepi, b_final;
   uint32_t tmem_slot;
   int err;
   int bad;
@@ -314,8 +316,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < nch; ++c) {
       const uint32_t ph = c & 1;
       const int k3 = c % 3;
-      // the prep warps' w-epilogue arrival orders their scalar writes before our reads
-      if (!(ok = vote_wait(&S.b_vn, ph) && vote_wait(&S.b_wepi, ph))) break;
+      // the previous output tile in sVN must have been read by its TMA store
+      if (t == 0) bulk_wait_read0();
+      // b_prep orders the prep warps' scalar writes of chunk c before our reads
+      if (!(ok = vote_wait(&S.b_prep, ph) && vote_wait(&S.b_w, ph))) break;
+      tc_fence_after();
+      // ---- w [d][i] (MN-major B operand) from w^T in TMEM (lane d, all 64 i)
+#pragma unroll
+      for (int colh = 0; colh < 2; ++colh) {
+        float r32[32];
+        tmem_ld32(lane_addr + TM_W + 32 * colh, r32);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) st_sw128_chunk(sWU, t, 4 * colh + q, pack8(r32 + 8 * q));
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar(kBarChain, 128);
+      if (t == 0) mbar_arrive(smem_u32(&S.b_wepi));
+      if (!(ok = vote_wait(&S.b_vn, ph))) break;
       tc_fence_after();
       // ---- vn^T [v][i] and vt^T [v][i] = vn * sv_i
 #pragma unroll
@@ -372,7 +391,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       named_bar(kBarChain, 128);
       if (t == 0) mbar_arrive(smem_u32(&S.b_state));
+      // ---- output of chunk c: o[r][v] = so_r o1[v][r] + o2[v][r] (lane v, all 64 rows).  A whole
+      //      chunk goes through sVN (free until the next v_new epilogue) and two TMA tensor stores; a
+      //      ragged last chunk is stored element by element so nothing past the sequence end is written.
+      {
+        const int64_t t0 = bos + (int64_t)c * C;
+        const int L = (int)(eos - t0 < C ? eos - t0 : C);
+        const int64_t rstride = p.HV * DV;
+#pragma unroll 1
+        for (int colh = 0; colh < 2; ++colh) {
+          float a32[32], b32[32], so[32];
+          tmem_ld32(lane_addr + TM_O1 + 32 * colh, a32);
+          tmem_ld32(lane_addr + TM_O2 + 32 * colh, b32);
+          ld_f32x32(S.so[k3] + 32 * colh, so);
+          tmem_ld_wait();
+          __nv_bfloat16 ov[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ov[j] = __float2bfloat16_rn(fmaf(so[j], a32[j], b32[j]));
+          if (L == C) {
+            uint8_t *tile = sVN + (t >> 6) * 8192;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              *reinterpret_cast<__nv_bfloat16 *>(tile + sw128_offset(32 * colh + j, t & 63)) = ov[j];
+          } else {
+            __nv_bfloat16 *ocol = p.o + (t0 * p.HV + hv) * DV + t + (int64_t)(32 * colh) * rstride;
+            const int nr = L - 32 * colh;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < nr) ocol[(int64_t)j * rstride] = ov[j];
+          }
+        }
+        tc_fence_before();
+        if (L == C) fence_proxy_async_smem();
+        named_bar(kBarChain, 128);
+        if (t == 0) {
+          if (L == C) {
+            tma_store_3d(&tm_o, smem_u32(sVN), 0, (int)hv, (int)t0);
+            tma_store_3d(&tm_o, smem_u32(sVN + 8192), 64, (int)hv, (int)t0);
+            bulk_commit();
+          }
+          mbar_arrive(smem_u32(&S.b_oepi));  // D_o1, D_o2 of chunk c have been read
+        }
+      }
     }
+    if (t == 0) bulk_wait0();  // every output store has landed before the block can exit
     if (named_bar_and(kBarChain, 128, ok && *err == 0) && p.ht) {
       float *dst = p.ht + (unit * DK + t) * DV;
 #pragma unroll
@@ -393,45 +455,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int colh = (warp - 4) >> 2;               // which half of the columns this warp reads
     const uint32_t lane_addr = tbase + ((uint32_t)(quad * 32) << 16);
     float *AT = reinterpret_cast<float *>(sm + OFF_AT);
-    uint8_t *const sO = sm + OFF_AT;  // bf16 output staging [r][v] (2 swizzled sub-tiles) once A / T are done
     auto vote_wait = [&](uint64_t *bar, uint32_t parity) -> bool {
       const bool ok = pt == 0 ? mbar_wait(smem_u32(bar), parity, err, tmo) : true;
       return named_bar_and(kBarPrep, kPrepThreads, ok);
-    };
-    // output of chunk cc: o[r][v] = so_r o1[v][r] + o2[v][r]; lane v, rows r of this half.  Whole
-    // chunks go through the staging tile and two TMA tensor stores; a ragged last chunk is
-    // stored element by element so nothing past the sequence end is written.
-    auto output_epilogue = [&](int cc) {
-      const int64_t t0 = bos + (int64_t)cc * C;
-      const int L = (int)(eos - t0 < C ? eos - t0 : C);
-      float a32[32], b32[32], so[32];
-      tmem_ld32(lane_addr + TM_O1 + 32 * colh, a32);
-      tmem_ld32(lane_addr + TM_O2 + 32 * colh, b32);
-      ld_f32x32(S.so[cc % 3] + 32 * colh, so);
-      tmem_ld_wait();
-      __nv_bfloat16 ov[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) ov[j] = __float2bfloat16_rn(fmaf(so[j], a32[j], b32[j]));
-      if (L == C) {
-        uint8_t *tile = sO + (lrow >> 6) * 8192;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          *reinterpret_cast<__nv_bfloat16 *>(tile + sw128_offset(32 * colh + j, lrow & 63)) = ov[j];
-        fence_proxy_async_smem();
-        named_bar(kBarPrep, kPrepThreads);
-        if (pt == 0) {
-          tma_store_3d(&tm_o, smem_u32(sO), 0, (int)hv, (int)t0);
-          tma_store_3d(&tm_o, smem_u32(sO + 8192), 64, (int)hv, (int)t0);
-          bulk_commit();
-        }
-      } else {
-        const int64_t rstride = p.HV * DV;
-        __nv_bfloat16 *ocol = p.o + (t0 * p.HV + hv) * DV + lrow + (int64_t)(32 * colh) * rstride;
-        const int nr = L - 32 * colh;  // rows of this half that exist
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < nr) ocol[(int64_t)j * rstride] = ov[j];
-      }
     };
     bool ok = true;
     for (int c = 0; c < nch; ++c) {
@@ -506,8 +532,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             S.factored = (g0 - gl) <= 160.f;
           }
         }
-        // the previous chunk's output staging (in the A / T array) must have been read by its TMA store
-        if (pt == 0) bulk_wait_read0();
       }
       named_bar(kBarPrep, kPrepThreads);
       const bool factored = S.factored;
@@ -576,11 +600,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       named_bar(kBarPrep, kPrepThreads);
       if (pt == 0) mbar_arrive(smem_u32(&S.b_prep));
-      // ---- output of chunk c-1 and P of chunk c, once MMA_o2(c-1) has consumed P(c-1)
+      // ---- P of chunk c, once MMA_o2(c-1) has consumed P(c-1)
       if (c > 0) {
         if (!(ok = vote_wait(&S.b_h, php))) break;
         tc_fence_after();
-        output_epilogue(c - 1);
       }
       if (quad >= 2) {
         const int r = lrow - 64;
@@ -592,29 +615,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       named_bar(kBarPrep, kPrepThreads);
-      // b_pend: P(c) is in place and D_o1, D_o2 of chunk c-1 have been read
+      // b_pend: P(c) is in place
       if (pt == 0) mbar_arrive(smem_u32(&S.b_pend));
-      // ---- w [d][i] (MN-major B operand) from w^T in TMEM (lane d, this half of i)
-      if (!(ok = vote_wait(&S.b_w, ph))) break;
-      tc_fence_after();
-      {
-        float r32[32];
-        tmem_ld32(lane_addr + TM_W + 32 * colh, r32);
-        tmem_ld_wait();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) st_sw128_chunk(sWU, lrow, 4 * colh + q, pack8(r32 + 8 * q));
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      named_bar(kBarPrep, kPrepThreads);
-      if (pt == 0) mbar_arrive(smem_u32(&S.b_wepi));
     }
-    // output of the last chunk
-    if (ok && nch > 0 && vote_wait(&S.b_h, (nch - 1) & 1)) {
-      tc_fence_after();
-      output_epilogue(nch - 1);
-    }
-    if (pt == 0) bulk_wait0();  // every output store has landed before the block can exit
+    (void)ok;
     tc_fence_before();
   } else if (warp == kProducerWarp) {
     // ================================================================ producer
@@ -677,13 +681,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t id_kk = idesc_bf16(128, 64, 0, 0);       // vn^T P^T
     const uint32_t aH = smem_u32(sH), aWU = smem_u32(sWU), aP = smem_u32(sP), aVN = smem_u32(sVN),
                    aVT = smem_u32(sVT), aV = smem_u32(sm + OFF_V);
-    auto wt = [&](uint64_t *bar, uint32_t parity) { return mbar_wait(smem_u32(bar), parity, err, tmo); };
+    auto wt = [&](uint64_t *bar, uint32_t parity) { return mbar_wait_spin(smem_u32(bar), parity, err, tmo); };
+    // Descriptors are built once: an operand at base + off (off a multiple of 16 bytes, every shared
+    // address below 2^18) has the base's descriptor plus off / 16 in its 14-bit address field.
+    auto at = [](uint64_t base, uint32_t off) { return base + (uint64_t)(off >> 4); };
+    const uint32_t aQK0 = smem_u32(sm + OFF_QK);
+    const uint64_t dQK0k = smem_desc(aQK0, 16, 1024), dQK0mn = smem_desc(aQK0, 16384, 1024);
+    const uint64_t dWUk = smem_desc(aWU, 16, 1024), dWUmn = smem_desc(aWU, 16384, 1024);
+    const uint64_t dVmn = smem_desc(aV, 8192, 1024), dHmn = smem_desc(aH, 16384, 1024);
+    const uint64_t dVTk = smem_desc(aVT, 16, 1024), dVNk = smem_desc(aVN, 16, 1024), dPk = smem_desc(aP, 16, 1024);
     auto issue_s = [&](int c) {
-      const uint32_t aQK = smem_u32(sm + OFF_QK + (c % kQKSlots) * SZ_QK);
+      const uint64_t qk = at(dQK0k, (uint32_t)(c % kQKSlots) * SZ_QK);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-        mma_bf16(tbase + TM_S, smem_desc(aQK + off, 16, 1024), smem_desc(aQK + off, 16, 1024), id_s, ks > 0);
+        mma_bf16(tbase + TM_S, at(qk, off), at(qk, off), id_s, ks > 0);
       }
       mma_commit(smem_u32(&S.b_s));
     };
@@ -693,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < nch; ++c) {
         const uint32_t ph = c & 1;
         const int slot = c % kQKSlots;
-        const uint32_t aQK = smem_u32(sm + OFF_QK + slot * SZ_QK);
+        const uint64_t qkk = at(dQK0k, (uint32_t)slot * SZ_QK), qkmn = at(dQK0mn, (uint32_t)slot * SZ_QK);
         // S of the next chunk as soon as the prep warps have read this one's
         if (c + 1 < nch) {
           if (!(wt(&S.b_sfree, ph) && wt(&S.full_qk[(c + 1) % kQKSlots], ((c + 1) / kQKSlots) & 1))) break;
@@ -705,34 +717,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          mma_bf16(tbase + TM_W, smem_desc(aQK + ks * 2048, 16384, 1024), smem_desc(aWU + ks * 32, 16, 1024),
-                   id_mnk, ks > 0);
-          mma_bf16(tbase + TM_VN, smem_desc(aV + ks * 2048, 8192, 1024),
-                   smem_desc(aWU + 8192 + ks * 32, 16, 1024), id_mnk, ks > 0);
+          mma_bf16(tbase + TM_W, at(qkmn, ks * 2048), at(dWUk, ks * 32), id_mnk, ks > 0);
+          mma_bf16(tbase + TM_VN, at(dVmn, ks * 2048), at(dWUk, 8192 + ks * 32), id_mnk, ks > 0);
         }
         mma_commit(smem_u32(&S.b_w));
         mma_commit(smem_u32(&S.empty_v));
-        // vn^T -= h^T w^T ; o1^T = h^T Q^T
-        if (!(wt(&S.b_wepi, ph) && wt(&S.b_state, ph) && wt(&S.b_pend, ph))) break;
+        // vn^T -= h^T w^T
+        if (!(wt(&S.b_wepi, ph) && wt(&S.b_state, ph))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_bf16(tbase + TM_VN, at(dHmn, ks * 2048), at(dWUmn, ks * 2048), id_vn, 1);
+        mma_commit(smem_u32(&S.b_vn));
+        // o1^T = h^T Q^T, once the chain has read chunk c-1's output accumulators
+        if (c > 0 && !wt(&S.b_oepi, (c - 1) & 1)) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          mma_bf16(tbase + TM_VN, smem_desc(aH + ks * 2048, 16384, 1024), smem_desc(aWU + ks * 2048, 16384, 1024),
-                   id_vn, 1);
           const uint32_t qoff = 8192 + (ks >> 2) * 16384 + (ks & 3) * 32;
-          mma_bf16(tbase + TM_O1, smem_desc(aH + ks * 2048, 16384, 1024), smem_desc(aQK + qoff, 16, 1024), id_mnk,
-                   ks > 0);
+          mma_bf16(tbase + TM_O1, at(dHmn, ks * 2048), at(qkk, qoff), id_mnk, ks > 0);
         }
-        mma_commit(smem_u32(&S.b_vn));
         // dH = K^T vt ; o2^T = vn^T P^T
-        if (!wt(&S.b_vnepi, ph ^ 1)) break;
+        if (!(wt(&S.b_vnepi, ph ^ 1) && wt(&S.b_pend, ph))) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          mma_bf16(tbase + TM_HS, smem_desc(aQK + ks * 2048, 16384, 1024), smem_desc(aVT + ks * 32, 16, 1024),
-                   id_h, 1);
-          mma_bf16(tbase + TM_O2, smem_desc(aVN + ks * 32, 16, 1024), smem_desc(aP + ks * 32, 16, 1024), id_kk,
-                   ks > 0);
+          mma_bf16(tbase + TM_HS, at(qkmn, ks * 2048), at(dVTk, ks * 32), id_h, 1);
+          mma_bf16(tbase + TM_O2, at(dVNk, ks * 32), at(dPk, ks * 32), id_kk, ks > 0);
         }
         mma_commit(smem_u32(&S.b_h));
         mma_commit(smem_u32(&S.empty_qk[slot]));

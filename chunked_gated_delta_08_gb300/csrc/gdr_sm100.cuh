@@ -93,6 +93,36 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Non-blocking test of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// The same bound with non-blocking polls: the waiting thread sees the phase
+// complete within a few cycles (the MMA issuer uses it; it costs issue slots,
+// so the roles doing arithmetic keep the sleeping form).
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile int *err, uint64_t max_cycles) {
+  const uint64_t t0 = clock64();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((i & 63u) == 63u) {
+      if (*err) return false;
+      if ((uint64_t)clock64() - t0 > max_cycles) {
+        *err = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // The same wait, ignoring the shared error flag (used while winding down to
 // let copies already in flight land before the block exits).
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t max_cycles) {
