@@ -72,6 +72,8 @@ constexpr int kThreads = 512;  // 16 warps: the last two only join the final bar
 constexpr int kBarChain = 1;   // named barrier of warps 0-3
 constexpr int kBarPrep = 2;    // named barrier of the prep warps
 constexpr int LDA = C + 1;     // row stride of the packed fp32 A / T^T matrix
+constexpr int kXL = 33;        // row stride of the solve scratch Y [32][kXL]
+constexpr int kZL = 18;        // row stride of the solve scratch Z [16][kZL] (two of them)
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr uint32_t SZ_QK = 32768;                    // [K d0-63 | Q d0-63 | K d64-127 | Q d64-127]
@@ -101,7 +103,7 @@ struct Small {
   float sv[3][C];               // chain: row scale of vt, rk_i e^{G_L - G_i} (0 past the end)
   float so[3][C];               // chain: row scale of o1, rq_r e^{G_r}
   float gL[4];                  // chain: G at the chunk's last valid row
-  float X[32 * 32];             // solve scratch
+  float X[32 * kXL];            // solve scratch
   uint64_t full_qk[kQKSlots], empty_qk[kQKSlots], full_v, empty_v;
   uint64_t b_s, b_sfree, b_prep, b_w, b_wepi, b_pend, b_vn, b_vnepi, b_h, b_state, b_oepi, b_scal, b_final;
   uint32_t tmem_slot;
@@ -140,19 +142,25 @@ __device__ __forceinline__ float t_at(const float *AT, int r, int s) {  // T[r][
 
 // D (16 x 8 tile at A-rows ar0.., B-cols bc0..) = A_tile(rows, k) * B(k, cols)
 // over nk k-steps of 8; A and B read through the functors fa(r, k), fb(k, n).
+// The sum over k is order-free, so fragment column t (and t + 4) of k-step ks
+// takes k = 2 nk t + 2 ks (+ 1): the four t of a load are 2 nk apart, so the
+// fragment loads from the odd-strided AT meet no shared-memory bank conflict at
+// nk = 4 and at most two-way ones at nk = 2 (k = t + 4 would be four-way).
 template <typename FA, typename FB>
 __device__ __forceinline__ void tile_product(float (&d)[4], int nk, FA fa, FB fb) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
 #pragma unroll
   for (int e = 0; e < 4; ++e) d[e] = 0.f;
   for (int ks = 0; ks < nk; ++ks) {
-    const int k0 = 8 * ks;
-    const float a[4] = {fa(g, k0 + t), fa(g + 8, k0 + t), fa(g, k0 + t + 4), fa(g + 8, k0 + t + 4)};
-    const float b[2] = {fb(k0 + t, g), fb(k0 + t + 4, g)};
+    const int k0 = 2 * nk * t + 2 * ks, k1 = k0 + 1;
+    const float a[4] = {fa(g, k0), fa(g + 8, k0), fa(g, k1), fa(g + 8, k1)};
+    const float b[2] = {fb(k0, g), fb(k1, g)};
     mma_3xtf32(d, a, b);
   }
 }
 
+// Row strides of the solve scratch: Y [32][kXL] and the two Z [16][kZL]; both
+// make the B-fragment loads of the permuted k (rows 2 nk apart) bank-conflict free.
 __device__ void solve_unit_lower(float *AT, float *X, int pt) {
   const int pw = pt >> 5, lane = pt & 31, g = lane >> 2, t = lane & 3;
   // ---- 16 x 16 diagonal blocks: prep warp b, lane c < 16 solves column c
@@ -177,22 +185,22 @@ __device__ void solve_unit_lower(float *AT, float *X, int pt) {
   // ---- 16 -> 32: T_{b,b-1} = -T_bb (A_{b,b-1} T_{b-1,b-1}) for b = 1, 3 (warps 0-3: pair, n-tile)
   if (pw < 4) {
     const int b = 1 + 2 * (pw >> 1), nt = pw & 1, r0 = 16 * b, c0 = 16 * (b - 1);
-    float *Z = X + (pw >> 1) * 256;  // Z [16][16]
+    float *Z = X + (pw >> 1) * 16 * kZL;  // Z [16][kZL]
     float d[4];
     tile_product(d, 2, [&](int r, int k) { return AT[(r0 + r) * LDA + c0 + k]; },
                  [&](int k, int n) { return t_at(AT, c0 + k, c0 + 8 * nt + n); });
-    Z[g * 16 + 8 * nt + 2 * t] = d[0];
-    Z[g * 16 + 8 * nt + 2 * t + 1] = d[1];
-    Z[(g + 8) * 16 + 8 * nt + 2 * t] = d[2];
-    Z[(g + 8) * 16 + 8 * nt + 2 * t + 1] = d[3];
+    Z[g * kZL + 8 * nt + 2 * t] = d[0];
+    Z[g * kZL + 8 * nt + 2 * t + 1] = d[1];
+    Z[(g + 8) * kZL + 8 * nt + 2 * t] = d[2];
+    Z[(g + 8) * kZL + 8 * nt + 2 * t + 1] = d[3];
   }
   named_bar(kBarPrep, kPrepThreads);
   if (pw < 4) {
     const int b = 1 + 2 * (pw >> 1), nt = pw & 1, r0 = 16 * b, c0 = 16 * (b - 1);
-    const float *Z = X + (pw >> 1) * 256;
+    const float *Z = X + (pw >> 1) * 16 * kZL;
     float d[4];
     tile_product(d, 2, [&](int r, int k) { return t_at(AT, r0 + r, r0 + k); },
-                 [&](int k, int n) { return Z[k * 16 + 8 * nt + n]; });
+                 [&](int k, int n) { return Z[k * kZL + 8 * nt + n]; });
     const int cc = c0 + 8 * nt + 2 * t;
     AT[cc * LDA + r0 + g] = -d[0];
     AT[(cc + 1) * LDA + r0 + g] = -d[1];
@@ -206,17 +214,17 @@ __device__ void solve_unit_lower(float *AT, float *X, int pt) {
     float d[4];
     tile_product(d, 4, [&](int r, int k) { return AT[(32 + 16 * mt + r) * LDA + k]; },
                  [&](int k, int n) { return t_at(AT, k, 8 * nt + n); });
-    X[(16 * mt + g) * 32 + 8 * nt + 2 * t] = d[0];
-    X[(16 * mt + g) * 32 + 8 * nt + 2 * t + 1] = d[1];
-    X[(16 * mt + g + 8) * 32 + 8 * nt + 2 * t] = d[2];
-    X[(16 * mt + g + 8) * 32 + 8 * nt + 2 * t + 1] = d[3];
+    X[(16 * mt + g) * kXL + 8 * nt + 2 * t] = d[0];
+    X[(16 * mt + g) * kXL + 8 * nt + 2 * t + 1] = d[1];
+    X[(16 * mt + g + 8) * kXL + 8 * nt + 2 * t] = d[2];
+    X[(16 * mt + g + 8) * kXL + 8 * nt + 2 * t + 1] = d[3];
   }
   named_bar(kBarPrep, kPrepThreads);
   {
     const int mt = pw >> 2, nt = pw & 3;
     float d[4];
     tile_product(d, 4, [&](int r, int k) { return t_at(AT, 32 + 16 * mt + r, 32 + k); },
-                 [&](int k, int n) { return X[k * 32 + 8 * nt + n]; });
+                 [&](int k, int n) { return X[k * kXL + 8 * nt + n]; });
     const int cc = 8 * nt + 2 * t, rr = 32 + 16 * mt + g;
     AT[cc * LDA + rr] = -d[0];
     AT[(cc + 1) * LDA + rr] = -d[1];
@@ -600,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- W' = T diag(beta e^G rk), U' = T diag(beta) into the w region once w(c-1) is consumed
       if (c > 0 && !(ok = vote_wait(&S.b_vn, php))) break;
       {
-        const int i = pt >> 2, j0 = 16 * (pt & 3);  // row i, columns j0 .. j0 + 15
+        const int i = pt & 63, j0 = 16 * (pt >> 6);  // row i, columns j0 .. j0 + 15
         float tv[16], bw[16], cw[16];
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) tv[jj] = t_at(AT, i, j0 + jj);
