@@ -146,6 +146,16 @@ __device__ __forceinline__ float t_at(const float *AT, int r, int s) {  // T[r][
 // takes k = 2 nk t + 2 ks (+ 1): the four t of a load are 2 nk apart, so the
 // fragment loads from the odd-strided AT meet no shared-memory bank conflict at
 // nk = 4 and at most two-way ones at nk = 2 (k = t + 4 would be four-way).
+// x = hi + lo with hi, lo tf32 bit patterns, by truncation (masking the low 13
+// mantissa bits) rather than conversion instructions, which keeps the split on
+// the integer and FMA pipes.  |lo| < 2^-10 |x| and lo is truncated in turn, so
+// hi*hi + hi*lo + lo*hi misses the product by under 2^-18 of it: fp32-like,
+// far below the bf16 rounding W' and U' get next.
+__device__ __forceinline__ void split_tf32_trunc(float x, uint32_t &hi, uint32_t &lo) {
+  hi = __float_as_uint(x) & 0xffffe000u;
+  lo = __float_as_uint(x - __uint_as_float(hi)) & 0xffffe000u;
+}
+
 template <typename FA, typename FB>
 __device__ __forceinline__ void tile_product(float (&d)[4], int nk, FA fa, FB fb) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -155,7 +165,14 @@ __device__ __forceinline__ void tile_product(float (&d)[4], int nk, FA fa, FB fb
     const int k0 = 2 * nk * t + 2 * ks, k1 = k0 + 1;
     const float a[4] = {fa(g, k0), fa(g + 8, k0), fa(g, k1), fa(g + 8, k1)};
     const float b[2] = {fb(k0, g), fb(k1, g)};
-    mma_3xtf32(d, a, b);
+    uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) split_tf32_trunc(a[e], ah[e], al[e]);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) split_tf32_trunc(b[e], bh[e], bl[e]);
+    mma_tf32(d, al[0], al[1], al[2], al[3], bh[0], bh[1]);
+    mma_tf32(d, ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
+    mma_tf32(d, ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
   }
 }
 
