@@ -85,8 +85,6 @@ int validate(const gdr_desc *d, int chunk_size, const int64_t *cu) {
   return GDR_OK;
 }
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 int64_t nt_max_of(const gdr_desc &d, int C, const int64_t *cu) {
   return cu ? nt_upper_bound(d, C) : d.B * cdiv(d.T, C);
 }

@@ -557,18 +557,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok = pt == 0 ? mbar_wait(smem_u32(bar), parity, err, tmo) : true;
       return named_bar_and(kBarPrep, kPrepThreads, ok);
     };
-    bool ok = true;
     for (int c = 0; c < nch; ++c) {
       const uint32_t ph = c & 1, php = (c - 1) & 1;
       const int slot = c % kQKSlots;
       const int64_t t0 = bos + (int64_t)c * C;
       const int L = (int)(eos - t0 < C ? eos - t0 : C);
       uint8_t *qk = sm + OFF_QK + slot * SZ_QK;
-      if (!(ok = vote_wait(&S.b_s, ph))) break;
+      if (!vote_wait(&S.b_s, ph)) break;
       tc_fence_after();
       // ragged tail: clear rows past the sequence end (they may hold the next sequence)
       if (L < C) {
-        if (!(ok = vote_wait(&S.full_v, ph))) break;
+        if (!vote_wait(&S.full_v, ph)) break;
         for (int e = pt; e < (C - L) * 48; e += kPrepThreads) {
           const int rr = L + e / 48, rest = e % 48, tile = rest >> 3, ch = rest & 7;
           uint8_t *base = tile < 4 ? qk + tile * 8192 : sm + OFF_V + (tile - 4) * 8192;
@@ -577,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
       }
       // ---- this chunk's norms, gate cumsum and scalars, from the chain warps
-      if (!(ok = vote_wait(&S.b_scal, ph))) break;
+      if (!vote_wait(&S.b_scal, ph)) break;
       const int par = c & 1;
       const bool factored = S.factored;
       // ---- A from lanes 0-63 of S: A_ij = beta_i rk_i rk_j e^{G_i - G_j} (k_i . k_j), i > j;
@@ -623,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- T = (I + A)^-1
       solve_unit_lower(AT, S.X, pt);
       // ---- W' = T diag(beta e^G rk), U' = T diag(beta) into the w region once w(c-1) is consumed
-      if (c > 0 && !(ok = vote_wait(&S.b_vn, php))) break;
+      if (c > 0 && !vote_wait(&S.b_vn, php)) break;
       {
         const int i = pt & 63, j0 = 16 * (pt >> 6);  // row i, columns j0 .. j0 + 15
         float tv[16], bw[16], cw[16];
@@ -647,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (pt == 0) mbar_arrive(smem_u32(&S.b_prep));
       // ---- P of chunk c, once MMA_o2(c-1) has consumed P(c-1)
       if (c > 0) {
-        if (!(ok = vote_wait(&S.b_h, php))) break;
+        if (!vote_wait(&S.b_h, php)) break;
         tc_fence_after();
       }
       if (quad >= 2) {
@@ -663,7 +662,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // b_pend: P(c) is in place
       if (pt == 0) mbar_arrive(smem_u32(&S.b_pend));
     }
-    (void)ok;
     tc_fence_before();
   } else if (warp == kProducerWarp) {
     // ================================================================ producer
