@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (c + 1 < nch && !(ok = scalars(c + 1))) break;
       // the previous output tile in sVN must have been read by its TMA store
       if (t == 0) bulk_wait_read0();
-      // b_prep orders the prep warps' scalar writes of chunk c before our reads
+      // w^T of chunk c is in TMEM (its MMAs follow the prep warps' b_prep arrival)
       if (!(ok = vote_wait(&S.b_prep, ph) && vote_wait(&S.b_w, ph))) break;
       tc_fence_after();
       // ---- w [d][i] (MN-major B operand) from w^T in TMEM (lane d, all 64 i)
@@ -546,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < 4 + kPrepWarps) {
-    // ================================================================ prep (+ output epilogue)
+    // ================================================================ prep
     const int pt = tid - 128;                       // 0..255
     const int quad = warp & 3;                      // TMEM lane quadrant
     const int lrow = quad * 32 + lane;              // TMEM lane of this thread
