@@ -9,13 +9,13 @@
 //
 //   S     = [K; Q] K^T                                tcgen05 M=128 N=64  K=128
 //   A_ij  = beta_i r_i r_j e^{G_i - G_j} (KK^T)_ij, i > j       (CUDA cores)
-//   T     = (I + A)^-1   blocked 16 x 16 inversion in fp32      (CUDA cores)
+//   T     = (I + A)^-1   16 x 16 blocks, then doubling   (CUDA cores, warp MMAs)
 //   W'    = T diag(beta e^G r),  U' = T diag(beta)              (bf16 operands)
 //   w^T   = K^T W'^T,  vn^T = V^T U'^T                 tcgen05 M=128 N=64  K=64
 //   vn^T -= h^T w^T,  o1^T = h^T Q^T                   tcgen05 M=128 N=64  K=128
 //   P_rj  = rq_r r_j e^{G_r - G_j} (QK^T)_rj, j <= r            (CUDA cores)
 //   dH    = K^T (vn * r e^{G_L - G}),  o2^T = vn^T P^T tcgen05 M=128 N=128/64 K=64
-//   h'    = e^{G_L} h + dH                             fp32, in registers
+//   h'    = e^{G_L} h + dH                             fp32, in TMEM
 //   o_r   = rq_r e^{G_r} o1_r + o2_r
 //
 // Every product has M = 128 (the K or V dimension), so an accumulator row is a
