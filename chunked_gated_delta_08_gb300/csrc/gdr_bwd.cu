@@ -27,6 +27,9 @@
 // Every decay factor is e^(G_i - G_j) with i >= j, e^(G_L - G_i) or e^(G_i),
 // so no exponent is positive for non-positive gates.  The backward keeps the
 // forward's chunk layouts and int64 addressing; it supports K <= 128.
+//
+// Pages cited: the coverage guide = "FLA 算子内核正确性测试与覆盖矩阵" (fla/ops correctness-coverage guide);
+//   the KCP handbook = "flash-linear-attention KCP 精度失效根因排查手册".
 #include "gdr_device.cuh"
 #include "gdr_internal.h"
 #include "gdr_prep.cuh"

@@ -19,6 +19,9 @@
 // Decay factors are always formed as exp(G_i - G_j) with i >= j, so every
 // exponent is <= 0 and nothing overflows, whatever the gate values.
 // All address arithmetic is int64 (coverage guide, section 四).
+//
+// Pages cited: the coverage guide = "FLA 算子内核正确性测试与覆盖矩阵" (fla/ops correctness-coverage guide);
+//   the KCP handbook = "flash-linear-attention KCP 精度失效根因排查手册".
 #include <algorithm>
 
 #include "gdr_device.cuh"

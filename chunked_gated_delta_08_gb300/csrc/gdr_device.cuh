@@ -1,4 +1,6 @@
 // gdr_device.cuh -- small device helpers shared by the kernels of libgdr.so.
+//
+// Pages cited: the coverage guide = "FLA 算子内核正确性测试与覆盖矩阵" (fla/ops correctness-coverage guide).
 #pragma once
 
 #include <cuda_bf16.h>

@@ -43,6 +43,8 @@
 //
 // Supported: bf16, scalar gate, K = V = 128, C = 64, dense or varlen.  Other
 // requests return GDR_ERR_UNSUPPORTED so the dispatcher takes the chunked form.
+//
+// Pages cited: the KCP handbook = "flash-linear-attention KCP 精度失效根因排查手册".
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>

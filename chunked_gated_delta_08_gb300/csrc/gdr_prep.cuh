@@ -7,6 +7,8 @@
 // Fragment layout of mma.sync m16n8k8 (g = lane / 4, t = lane % 4): A (16x8)
 // (g, t) (g+8, t) (g, t+4) (g+8, t+4); B (8x8, K x N) (t, g) (t+4, g);
 // D (16x8) (g, 2t) (g, 2t+1) (g+8, 2t) (g+8, 2t+1).
+//
+// Pages cited: the coverage guide = "FLA 算子内核正确性测试与覆盖矩阵" (fla/ops correctness-coverage guide).
 #pragma once
 
 #include "gdr_scan.cuh"

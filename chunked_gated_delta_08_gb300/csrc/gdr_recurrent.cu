@@ -16,6 +16,8 @@
 // end by the same block, so ht may alias h0 (in-place decode).  With the
 // varlen layout, cu_seqlens is first checked by the chunk-index kernel; on a
 // violation nothing is written.
+//
+// Pages cited: the coverage guide = "FLA 算子内核正确性测试与覆盖矩阵" (fla/ops correctness-coverage guide).
 #include "gdr_device.cuh"
 #include "gdr_internal.h"
 

@@ -15,6 +15,8 @@
 //   hs [Kp][kHS]   state tile          ws [C][Kp + 4]  -w
 //   kt [C][Kp + 8] Kb                  vn [C][kHS]     v_new
 //   gl [Kp]        G_L per key row
+//
+// Pages cited: the KCP handbook = "flash-linear-attention KCP 精度失效根因排查手册".
 #pragma once
 
 #include "gdr_device.cuh"

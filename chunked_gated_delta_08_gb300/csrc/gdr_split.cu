@@ -21,6 +21,8 @@
 // then the chunked fwd_o.  The sequential depth falls from a sequence's chunk
 // count to one segment's chunks plus its segment count, at about three times
 // the state-scan arithmetic.
+//
+// Pages cited: the KCP handbook = "flash-linear-attention KCP 精度失效根因排查手册".
 #include "gdr_device.cuh"
 #include "gdr_internal.h"
 #include "gdr_scan.cuh"

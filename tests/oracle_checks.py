@@ -17,6 +17,8 @@ checks can be run against deliberately broken copies of the oracle (see
   the scalar GDN gate;
 * the chunk form (UT transform): v_new = u - w h, h' = e^{G_C} h +
   (K * e^{G_C - G})^T v_new, o from the inter + intra terms.
+
+Pages cited: the coverage guide = "FLA 算子内核正确性测试与覆盖矩阵" (fla/ops correctness-coverage guide).
 """
 from __future__ import annotations
 

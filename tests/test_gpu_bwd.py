@@ -8,6 +8,8 @@ must each be within relative L2 error 5e-3 (the coverage guide's assert_close
 bar, section 三).  fp32 inputs are held to 1e-5.  The other cases cover the
 scalar gate, grouped value heads, K != V, chunk size 32, partial and empty
 sequences, and missing dht / h0.
+
+Pages cited: the coverage guide = "FLA 算子内核正确性测试与覆盖矩阵" (fla/ops correctness-coverage guide).
 """
 import numpy as np
 import pytest

@@ -5,6 +5,8 @@ inputs, on o and ht (the 0.005 assert_close bar of the coverage guide,
 section 三; the fp32 bar is the tighter one set for fp32 inputs).  The metric is
 ||x - ref||_2 / ||ref||_2 over the whole tensor (FLA contributor guide,
 section Testing: RMS(diff) / RMS(ref)), with any NaN a failure.
+
+Pages cited: the coverage guide = "FLA 算子内核正确性测试与覆盖矩阵" (fla/ops correctness-coverage guide); the contributor guide = "Flash Linear Attention 贡献者指南".
 """
 import numpy as np
 import pytest

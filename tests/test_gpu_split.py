@@ -3,6 +3,8 @@ oracle: sequences cut into 1024-token segments, each segment's transition M
 and zero-start end state S_ext, the merge S_in(s+1) = M_s S_in(s) + S_ext,s,
 then the segments rescanned from their true entering states (the KCP
 handbook's segment merge, on one GPU).  Tolerances as for the other forms.
+
+Pages cited: the KCP handbook = "flash-linear-attention KCP 精度失效根因排查手册".
 """
 import numpy as np
 import pytest

@@ -9,6 +9,8 @@ form through the C ABI against the oracle.
   sums, so no gate bound is assumed; these cases check that with gates far
   stronger than the workloads' (log-decays down to about -100 per token,
   whose products underflow to zero) and with gates that change sign.
+
+Pages cited: the coverage guide = "FLA 算子内核正确性测试与覆盖矩阵" (fla/ops correctness-coverage guide).
 """
 import numpy as np
 import pytest

@@ -1,4 +1,7 @@
-"""The oracle against facts outside itself (CPU only)."""
+"""The oracle against facts outside itself (CPU only).
+
+Pages cited: the KCP handbook = "flash-linear-attention KCP 精度失效根因排查手册".
+"""
 import json
 import os
 
