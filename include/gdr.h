@@ -201,7 +201,10 @@ int gdr_chunk_fwd_o(const gdr_desc *desc, const void *q, const void *k, const fl
  * K = V = 128, so e.g. 1024 tokens x 16 heads fit).
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before any
- *     stream capture.
+ *     stream capture.  The address is kept for the life of the process: it
+ *     does not survive cudaDeviceReset (or any other teardown of the device's
+ *     primary context), after which this entry point must not be called
+ *     again in the same process.
  *   - Every call shares the one array: calls whose work overlaps on the GPU
  *     (concurrent streams, or several host threads) race and corrupt each
  *     other's results; serialize them.  Every scratch byte a call reads it

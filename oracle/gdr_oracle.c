@@ -21,8 +21,7 @@
  * The scalar-gate case (GDN) uses D = exp(g_t) I; the per-key-channel case
  * (KDA) uses D = Diag(exp g_t[0..K-1]), scaling row d of S.
  *
- * Readings where the pages leave a step open (each is also listed in the
- * design notes):
+ * Readings where the pages leave a step open:
  *   - in-kernel L2 norm: x / sqrt(sum x^2 + 1e-6), applied to q and k per
  *     token and head ("use_qk_l2norm_in_kernel" axis, coverage guide section 三);
  *   - grouped value heads: value head hv reads q/k head hv / (HV / H)

@@ -87,6 +87,24 @@ def test_split_long_sequence_sampled_heads(gdr):
     assert eo <= 5e-3 and eh <= 5e-3, f"o {eo:.2e} ht {eh:.2e}"
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+@pytest.mark.parametrize("per_k", [False, True], ids=["gdn", "kda"])
+@pytest.mark.parametrize("C", [32, 64])
+def test_split_single_segment_is_bit_exact(gdr, dtype, per_k, C):
+    """A uniform single sequence no longer than one 1024-token segment: there is
+    nothing to merge (the segment starts from h0 itself), so the split must give
+    exactly the bits of the unsplit chunked form (the KCP handbook, TL;DR step 4:
+    a uniform single sequence is bit-perfect between the split and unsplit runs).
+    Dense batches of such sequences and a varlen batch of short ones too."""
+    for B, T, lengths in ((1, 1024, None), (1, 1000, None), (3, 700, None), (1, 1500, (1024, 5, 0, 471))):
+        w, x = wl.random_case(B, T, 2, 4, 64, 48, dtype=dtype, lengths=lengths, gate_per_k=per_k, use_h0=True,
+                              seed=55)
+        o_s, ht_s = run(gdr, x, True, C=C, algo="split")
+        o_c, ht_c = run(gdr, x, True, C=C, algo="chunked")
+        assert torch.equal(o_s, o_c), f"B={B} T={T} lengths={lengths}: o differs"
+        assert torch.equal(ht_s, ht_c), f"B={B} T={T} lengths={lengths}: ht differs"
+
+
 def test_split_bad_cu_seqlens_touches_nothing(gdr):
     w, x = wl.random_case(1, 2000, 1, 1, 32, 32, dtype=torch.float32, lengths=(1500, 500), seed=53)
     d = {n: dev(t) for n, t in x.items()}

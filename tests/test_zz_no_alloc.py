@@ -38,18 +38,48 @@ def _noalloc(gdr, d, C, l2):
     return o, ht
 
 
+def _fwd_chunked(gdr, d, C, l2):
+    o, ht = gdr.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0=d["h0"], cu_seqlens=d["cu_seqlens"],
+                    chunk_size=C, use_qk_l2norm=l2, algo="chunked")
+    torch.cuda.synchronize()
+    return o, ht
+
+
+def _dev(x):
+    return {k: (None if t is None else t.cuda()) for k, t in x.items()}
+
+
 @pytest.mark.gpu
 def test_noalloc_matches_gdr_fwd_on_two_calls_in_a_row(gdr):
-    cases = [(wl.GDN_BF16_VARLEN, None), (wl.GDN_BF16_GVA_K60, None)]
-    for w, _ in cases:
-        x = wl.make_inputs(w)
-        d = {k: (None if t is None else t.cuda()) for k, t in x.items()}
-        o_ref, ht_ref = gdr.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0=d["h0"], cu_seqlens=d["cu_seqlens"],
-                                chunk_size=w.chunk_size, use_qk_l2norm=w.use_qk_l2norm, algo="chunked")
-        torch.cuda.synchronize()
+    """The same kernels on the same inputs as gdr_fwd's chunked form, so the
+    results must be identical bit for bit: on two workloads of different shapes,
+    then on one shape twice with different inputs (nothing may carry over from
+    the previous call's contents of the shared array)."""
+    runs = [(wl.GDN_BF16_VARLEN, None), (wl.GDN_BF16_GVA_K60, None), (wl.GDN_BF16_GVA_K60, 7)]
+    for w, seed in runs:
+        d = _dev(wl.make_inputs(w, seed=seed))
+        o_ref, ht_ref = _fwd_chunked(gdr, d, w.chunk_size, w.use_qk_l2norm)
         o, ht = _noalloc(gdr, d, w.chunk_size, w.use_qk_l2norm)
         assert torch.isfinite(o.float()).all() and torch.isfinite(ht).all()
-        assert _rel(o, o_ref) <= TOL[w.dtype] and _rel(ht, ht_ref) <= TOL[w.dtype], w.name
+        assert torch.equal(o, o_ref) and torch.equal(ht, ht_ref), (w.name, seed)
+        # and within the parity tolerance of the other tests, for the record
+        assert _rel(o, o_ref) <= TOL[w.dtype] and _rel(ht, ht_ref) <= TOL[w.dtype]
+
+
+@pytest.mark.gpu
+def test_noalloc_bad_cu_seqlens_leaves_outputs_untouched(gdr):
+    """cu_seqlens that decrease: nothing is written (there is no status word on
+    this path, so the NaN-filled outputs are the evidence)."""
+    w, x = wl.random_case(1, 2000, 1, 1, 32, 32, dtype=torch.float32, lengths=(1500, 500), seed=53)
+    d = _dev(x)
+    d["cu_seqlens"] = torch.tensor([0, 1600, 1500], dtype=torch.int64, device="cuda")
+    o, ht = _noalloc(gdr, d, 64, True)
+    assert torch.isnan(o).all() and torch.isnan(ht).all()
+    # a good call right after still matches gdr_fwd exactly
+    d = _dev(x)
+    o_ref, ht_ref = _fwd_chunked(gdr, d, 64, True)
+    o, ht = _noalloc(gdr, d, 64, True)
+    assert torch.equal(o, o_ref) and torch.equal(ht, ht_ref)
 
 
 def test_noalloc_rejects_requests_beyond_its_array(gdr):
