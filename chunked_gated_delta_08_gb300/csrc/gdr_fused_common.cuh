@@ -31,7 +31,18 @@ __device__ __forceinline__ uint4 ld_sw128_chunk(const uint8_t *tile, uint32_t ro
   return *reinterpret_cast<const uint4 *>(tile + sw128_chunk_off(row, chunk));
 }
 
-// Batched vector loads of 16 / 32 consecutive floats (16-byte aligned).
+// Batched vector loads of 8 / 16 / 32 consecutive floats (16-byte aligned).
+__device__ __forceinline__ void ld_f32x8(const float *src, float (&d)[8]) {
+  const float4 a = reinterpret_cast<const float4 *>(src)[0], b = reinterpret_cast<const float4 *>(src)[1];
+  d[0] = a.x;
+  d[1] = a.y;
+  d[2] = a.z;
+  d[3] = a.w;
+  d[4] = b.x;
+  d[5] = b.y;
+  d[6] = b.z;
+  d[7] = b.w;
+}
 __device__ __forceinline__ void ld_f32x16(const float *src, float (&d)[16]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {

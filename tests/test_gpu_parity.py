@@ -169,6 +169,22 @@ def test_unit_grid(gdr, case, C, dtype, algo):
         assert_parity(o, ht, ref, dtype, f"{case} C={C} l2={l2} h0={use_h0}")
 
 
+# ---------------------------------------------------------------- fused form, weak and strong decay
+@pytest.mark.parametrize("gate_div", [1.0, 16.0, 256.0])
+@pytest.mark.parametrize("lengths", [None, (1000, 17, 64, 300)], ids=["dense", "varlen"])
+def test_fused_decay_regimes(gdr, gate_div, lengths):
+    """The fused tensor-core kernel where the chunk's off-diagonal blocks of A
+    and T carry weight (weak decay: g = logsigmoid(N(0,1)) / 256) as well as
+    where they vanish (g = logsigmoid(N(0,1))), with an initial state, the
+    in-kernel L2 norm and partial last chunks."""
+    B = 1 if lengths else 2
+    T = sum(lengths) if lengths else 700
+    _, x = wl.random_case(B, T, 2, 4, 128, 128, dtype=torch.bfloat16, lengths=lengths, use_h0=True, seed=61,
+                          gate_div=gate_div)
+    o, ht = run_gpu(gdr, x, 64, True, "fused")
+    assert_parity(o, ht, run_ref(x, True), torch.bfloat16, f"gate_div={gate_div}")
+
+
 # ---------------------------------------------------------------- over-read detection
 @pytest.mark.parametrize("per_k,D", [(False, 60), (True, 60), (False, 128)])
 def test_padding_poison_detects_overreads(gdr, per_k, D):
