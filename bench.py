@@ -18,7 +18,10 @@ also carries ``bwd``: the backward timed on the KDA varlen workload (lengths
 ``decode``: one decode step of the per-token form (256 sequences x 1 token,
 32 heads, K = V = 128, state in place) against HBM bandwidth; and ``split``:
 the intra-sequence split on one 32768-token fp32 sequence with 4 heads,
-beside the unsplit chunked form.
+beside the unsplit chunked form; and ``configs``: the forward on each other
+configuration (fp32 T=128 K=V=64; bf16 K=V=60 with grouped values; the varlen
+400/624 pair; the KDA varlen case), each against the method's roofline, with
+its chunked-form kernels timed one by one where that form serves it.
 """
 from __future__ import annotations
 
@@ -413,6 +416,59 @@ def split_measurement(gdr, steps: int, warmup: int = 3):
                          "algorithmic_bytes_per_launch": byt}}
 
 
+def configs_measurement(gdr, steps: int, warmup: int = 3):
+    """The forward on every other configuration (the fp32 small case, K = V = 60
+    with grouped values, the varlen pair, the KDA varlen case), each with its
+    roofline by the method's definition and against measured HBM, and, where
+    the chunked form serves it, the duration of each of its kernels.  Inputs
+    resident; L2 flushed by a 256 MB write before every timed step (these
+    inputs fit in L2)."""
+    pk = peaks()
+    flush = torch.empty(64 << 20, dtype=torch.float32, device="cuda")
+    s = torch.cuda.current_stream()
+    out = {}
+    for w in (wl.GDN_FP32_SMALL, wl.GDN_BF16_GVA_K60, wl.GDN_BF16_VARLEN, wl.KDA_BF16_VARLEN):
+        x = wl.make_inputs(w)
+        d = {k: (None if t is None else t.cuda()) for k, t in x.items()}
+        o = torch.empty(w.B, w.T, w.HV, w.V, dtype=w.dtype, device="cuda")
+        ht = torch.empty(w.N, w.HV, w.K, w.V, dtype=torch.float32, device="cuda")
+
+        def call():
+            gdr.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0=d["h0"], cu_seqlens=d["cu_seqlens"],
+                    chunk_size=w.chunk_size, use_qk_l2norm=w.use_qk_l2norm, out=o, final_state=ht)
+
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize()
+        l0 = gdr.launch_count()
+        ms = []
+        for _ in range(steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            call()
+            e1.record(s)
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        launches = (gdr.launch_count() - l0) / steps
+        if gdr.device_status() != 0:
+            raise RuntimeError(f"device status after {w.name}: {gdr.last_error()}")
+        avg = statistics.median(ms)
+        byt, flops = algorithmic_bytes(w), algorithmic_flops(w)
+        spec_us = max(byt / (NOMINAL_HBM_GBS * 1e9), flops / (pk["bf16_tflops"] * 1e12)) * 1e6
+        kernels = None
+        if launches > 1.0 + 1e-9:
+            kernels, _ = stage_timings(gdr, w, d, 3)
+        out[w.name] = {"value": w.B * w.T / (avg * 1e-3), "unit": UNIT, "ms_per_step": avg, "steps": steps,
+                       "gpu_launches_per_step": launches, "form": "fused" if launches <= 1.0 + 1e-9 else "chunked",
+                       "l2_flush": "256 MB write before every step", "kernel_ms": kernels,
+                       "roofline_spec": {"bytes": byt, "flops": flops, "roofline_us": spec_us,
+                                         "frac": spec_us / (avg * 1e3),
+                                         "frac_of_measured_hbm": (byt / (pk["hbm_gbs"] * 1e9)) / (avg * 1e-3)}}
+        del d, o, ht
+    return out
+
+
 def profile_pass(gdr):
     """Every form once on a mid-size workload, for a per-kernel ncu capture:
     fused, chunked and split forwards on one 32768-token GDN sequence with 32
@@ -543,6 +599,9 @@ def run_ours(args, w, world, rank, local):
     split = None
     if rank == 0 and world == 1 and not args.no_split:
         split = split_measurement(gdr, steps=max(1, min(args.steps, 3)))
+    configs = None
+    if rank == 0 and world == 1 and not args.no_configs:
+        configs = configs_measurement(gdr, steps=max(3, min(args.steps, 10)))
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -553,7 +612,7 @@ def run_ours(args, w, world, rank, local):
                         "d2h_bytes_per_step": d2h},
                 "gpu_launches": launches, "roofline": roofline, "roofline_spec": roofline_spec,
                 "cpu_baseline": cpu, "step_ms": {"min": min(step_ms), "median": statistics.median(step_ms)},
-                "bwd": bwd, "decode": decode, "split": split}
+                "bwd": bwd, "decode": decode, "split": split, "configs": configs}
         print(json.dumps(line), flush=True)
 
 
@@ -569,7 +628,8 @@ def main():
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward measurement")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
     ap.add_argument("--no-split", action="store_true", help="skip the intra-sequence split measurement")
-    ap.add_argument("--mode", default="fwd", choices=["fwd", "bwd", "decode", "split", "profile"],
+    ap.add_argument("--no-configs", action="store_true", help="skip the forward on the other configurations")
+    ap.add_argument("--mode", default="fwd", choices=["fwd", "bwd", "decode", "split", "configs", "profile"],
                     help="bwd / decode: run only that measurement and print it alone")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
@@ -579,7 +639,8 @@ def main():
         if args.mode == "profile":
             print(json.dumps({"mode": "profile", **profile_pass(gdr)}), flush=True)
             return
-        fn = {"bwd": bwd_measurement, "decode": decode_measurement, "split": split_measurement}[args.mode]
+        fn = {"bwd": bwd_measurement, "decode": decode_measurement, "split": split_measurement,
+              "configs": configs_measurement}[args.mode]
         res = fn(gdr, steps=args.steps, warmup=args.warmup)
         print(json.dumps({"mode": args.mode, **res}), flush=True)
         return
