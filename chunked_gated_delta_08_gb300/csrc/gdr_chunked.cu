@@ -6,8 +6,8 @@
 //   chunk_index_kernel  cu_seqlens -> (sequence, chunk) map, int64
 //   prepare_kernel      per (chunk, value head): L2 norm of k, gate cumsum,
 //                       A = tril(beta K K^T * decay, -1), T = (I + A)^-1 by
-//                       blocks, w and u as products with T (tensor cores,
-//                       3 x TF32)
+//                       blocks (tensor cores, 3 x TF32), w and u as products
+//                       with T
 //   fwd_h_kernel        per (sequence, value head, V-tile), sequential over
 //                       chunks: h (state entering the chunk), v_new = u - w h,
 //                       h <- exp(G_C) h + (K * exp(G_C - G))^T v_new, both
@@ -18,6 +18,13 @@
 //
 // Decay factors are always formed as exp(G_i - G_j) with i >= j, so every
 // exponent is <= 0 and nothing overflows, whatever the gate values.
+//
+// Precision by input type: fp32 inputs take every product in 3 x TF32 (close
+// to fp32) and the full-precision exponential.  bf16 inputs keep 3 x TF32 for
+// the Gram matrices and the solve (T feeds every later product), and take
+// the products the fused form also runs in bf16 -- w, u = T [..], v_new = u -
+// w h, the state update, q h and P v_new -- as single-pass bf16 warp MMAs
+// (m16n8k16, fp32 accumulation), with the hardware exponential.
 // All address arithmetic is int64 (coverage guide, section 四).
 //
 // Pages cited: the coverage guide = "FLA 算子内核正确性测试与覆盖矩阵" (fla/ops correctness-coverage guide);
@@ -187,10 +194,7 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(
       }
     }
   }
-  for (int64_t e = tid; e < C * gw; e += kThreads) {
-    const int64_t i = e / gw, d = e % gw;
-    gam[i * GL + d] = i < Lc ? g[((t0 + i) * HV + hv) * gw + d] : 0.f;
-  }
+  prep::tile_to_smem(gam, GL, g + (t0 * HV + hv) * gw, HV * gw, C, (int)gw, Lc, (int)gw);
   for (int i = tid; i < C; i += kThreads) bet[i] = i < Lc ? load_beta(beta, (t0 + i) * HV + hv, beta_logits) : 0.f;
   __syncthreads();
   for (int64_t d = tid; d < gw; d += kThreads) {  // inclusive cumsum down each column
@@ -201,13 +205,11 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(
     }
   }
   __syncthreads();
-  for (int64_t e = tid; e < Lc * gw; e += kThreads) {
-    const int64_t i = e / gw, d = e % gw;
-    gcum[((t0 + i) * HV + hv) * gw + d] = gam[i * GL + d];
-  }
+  for (prep::Walk2D wk(tid, kThreads, (int)gw); wk.r < Lc; wk.next())
+    gcum[((t0 + wk.r) * HV + hv) * gw + wk.c] = gam[wk.r * GL + wk.c];
 
   // ---- A (strictly lower) into AT
-  prep::decayed_gram<C, PER_K, true>(ks, ks, KL, gam, GL, K, Lc, bet, AT, LA, Xs, Ys);
+  prep::decayed_gram<C, PER_K, true, scan::kB16<Tin>>(ks, ks, KL, gam, GL, K, Lc, bet, AT, LA, Xs, Ys);
 
   // ---- T = (I + A)^-1, then dense into Tm (row-major, diagonal 1)
   prep::solve_unit_lower<C>(AT, LA, Bt);
@@ -220,21 +222,34 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(
   const int64_t ncol = K + V;
   for (int64_t c0 = 0; c0 < ncol; c0 += kBtCols) {
     __syncthreads();  // Tm complete; the previous tile's reads of Bt done
-    for (int e = tid; e < C * kBtCols; e += kThreads) {
-      const int jj = e / kBtCols, cc = e % kBtCols;
-      const int64_t col = c0 + cc;
-      float x = 0.f;
-      if (jj < Lc && col < ncol) {
-        if (col < K) x = bet[jj] * expf(PER_K ? gam[jj * GL + col] : gam[jj]) * ks[jj * KL + col];
-        else x = bet[jj] * to_f32(v[((t0 + jj) * HV + hv) * V + (col - K)]);
+    // eight elements per thread in flight: their v loads are issued before any is used
+    for (int e0 = tid; e0 < C * kBtCols; e0 += 8 * kThreads) {
+      float x[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int e = e0 + q * kThreads, jj = e / kBtCols, cc = e % kBtCols;
+        const int64_t col = c0 + cc;
+        x[q] = (e < C * kBtCols && jj < Lc && col >= K && col < ncol) ? to_f32(v[((t0 + jj) * HV + hv) * V + (col - K)])
+                                                                    : 0.f;
       }
-      Bt[jj * kBtLd + cc] = x;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int e = e0 + q * kThreads, jj = e / kBtCols, cc = e % kBtCols;
+        const int64_t col = c0 + cc;
+        if (e >= C * kBtCols) break;
+        float y = 0.f;
+        if (jj < Lc && col < ncol)
+          y = col < K ? bet[jj] * scan::exp_<scan::kB16<Tin>>(PER_K ? gam[jj * GL + col] : gam[jj]) * ks[jj * KL + col]
+                      : bet[jj] * x[q];
+        Bt[jj * kBtLd + cc] = y;
+      }
     }
     __syncthreads();
     for (int tix = warp; tix < (C / 16) * (kBtCols / 8); tix += kWarps) {
       const int m0 = 16 * (tix % (C / 16)), n0 = 8 * (tix / (C / 16));
       float d[4];
-      prep::tile<false>(d, Tm, LT, Bt, kBtLd, m0, n0, C / 8);
+      if constexpr (scan::kB16<Tin>) prep::tile_b16<false>(d, Tm, LT, Bt, kBtLd, m0, n0, C / 16);
+      else prep::tile<false>(d, Tm, LT, Bt, kBtLd, m0, n0, C / 8);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = m0 + gq + 8 * (e >> 1);
@@ -340,36 +355,32 @@ __global__ void __launch_bounds__(kThreads) fwd_o_kernel(
   const int64_t gw = PER_K ? K : 1;
 
   prep::load_qk_rows<Tin, C>(q, k, t0, Lc, H, hq, K, l2, qs, ks, KL);
-  for (int64_t e = tid; e < C * gw; e += kThreads) {
-    const int64_t i = e / gw, d = e % gw;
-    gam[i * GL + d] = i < Lc ? gcum[((t0 + i) * HV + hv) * gw + d] : 0.f;
-  }
+  prep::tile_to_smem(gam, GL, gcum + (t0 * HV + hv) * gw, HV * gw, C, (int)gw, Lc, (int)gw);
   for (int e = tid; e < C * LP; e += kThreads) P[e] = 0.f;  // the product reads P's upper part too
   __syncthreads();
-  prep::decayed_gram<C, PER_K, false>(qs, ks, KL, gam, GL, K, Lc, nullptr, P, LP, Xs, Ys);
+  prep::decayed_gram<C, PER_K, false, scan::kB16<Tin>>(qs, ks, KL, gam, GL, K, Lc, nullptr, P, LP, Xs, Ys);
   // q * e^G in place
-  for (int64_t e = tid; e < C * Kp; e += kThreads) {
-    const int i = (int)(e / Kp);
-    const int64_t d = e % Kp;
-    if (d < K) qs[i * KL + d] *= expf(PER_K ? gam[i * GL + d] : gam[i]);
+  for (prep::Walk2D wk(tid, kThreads, (int)Kp); wk.r < C; wk.next()) {
+    const int i = wk.r, d = wk.c;
+    if (d < K) qs[i * KL + d] *= scan::exp_<scan::kB16<Tin>>(PER_K ? gam[i * GL + d] : gam[i]);
   }
 
   for (int64_t v0 = 0; v0 < V; v0 += kOCols) {
     __syncthreads();  // q * e^G done; the previous tile's reads of hs and vn done
-    for (int64_t e = tid; e < Kp * kOCols; e += kThreads) {
-      const int64_t d = e / kOCols, vv = e % kOCols;
-      hs[d * kOLd + vv] = (d < K && v0 + vv < V) ? h[((chunk * HV + hv) * K + d) * V + v0 + vv] : 0.f;
-    }
-    for (int e = tid; e < C * kOCols; e += kThreads) {
-      const int i = e / kOCols, vv = e % kOCols;
-      vn[i * kOLd + vv] = (i < Lc && v0 + vv < V) ? v_new[((t0 + i) * HV + hv) * V + v0 + vv] : 0.f;
-    }
+    const int vok = (int)(V - v0 < kOCols ? V - v0 : kOCols);
+    prep::tile_to_smem(hs, kOLd, h + (chunk * HV + hv) * K * V + v0, V, (int)Kp, kOCols, (int)K, vok);
+    prep::tile_to_smem(vn, kOLd, v_new + (t0 * HV + hv) * V + v0, HV * V, C, kOCols, Lc, vok);
     __syncthreads();
     for (int tix = warp; tix < (C / 16) * (kOCols / 8); tix += kWarps) {
       const int m0 = 16 * (tix % (C / 16)), n0 = 8 * (tix / (C / 16));
       float d1[4], d2[4];
-      prep::tile<false>(d1, qs, KL, hs, kOLd, m0, n0, (int)(Kp / 8));
-      prep::tile<false>(d2, P, LP, vn, kOLd, m0, n0, C / 8);
+      if constexpr (scan::kB16<Tin>) {
+        prep::tile_b16<false>(d1, qs, KL, hs, kOLd, m0, n0, (int)(Kp / 16));
+        prep::tile_b16<false>(d2, P, LP, vn, kOLd, m0, n0, C / 16);
+      } else {
+        prep::tile<false>(d1, qs, KL, hs, kOLd, m0, n0, (int)(Kp / 8));
+        prep::tile<false>(d2, P, LP, vn, kOLd, m0, n0, C / 8);
+      }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = m0 + gq + 8 * (e >> 1);

@@ -46,6 +46,38 @@ __device__ __forceinline__ void tile(float (&d)[4], const float *a, int64_t lda,
   }
 }
 
+// The same product in one bf16 pass (m16n8k16, fp32 accumulation; operands
+// rounded to bf16 as they are read), over 16 nk16 values of k, for the bf16
+// path's products whose operands the fused form also takes in bf16.  A rows
+// and (TB) B rows must start on 8-byte boundaries (even strides and offsets).
+template <bool TB>
+__device__ __forceinline__ void tile_b16(float (&d)[4], const float *a, int64_t lda, const float *b, int64_t ldb,
+                                         int m0, int n0, int nk16) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) d[e] = 0.f;
+  for (int ks = 0; ks < nk16; ++ks) {
+    const int k0 = 16 * ks;
+    const float *ar = a + (int64_t)(m0 + g) * lda + k0 + 2 * t;
+    const float2 x0 = *reinterpret_cast<const float2 *>(ar), x1 = *reinterpret_cast<const float2 *>(ar + 8 * lda),
+                 x2 = *reinterpret_cast<const float2 *>(ar + 8),
+                 x3 = *reinterpret_cast<const float2 *>(ar + 8 * lda + 8);
+    uint32_t b0, b1;
+    if (TB) {
+      const float *br = b + (int64_t)(n0 + g) * ldb + k0 + 2 * t;
+      const float2 y0 = *reinterpret_cast<const float2 *>(br), y1 = *reinterpret_cast<const float2 *>(br + 8);
+      b0 = scan::bf16x2(y0.x, y0.y);
+      b1 = scan::bf16x2(y1.x, y1.y);
+    } else {
+      const float *br = b + (int64_t)(k0 + 2 * t) * ldb + n0 + g;
+      b0 = scan::bf16x2(br[0], br[ldb]);
+      b1 = scan::bf16x2(br[8 * ldb], br[9 * ldb]);
+    }
+    scan::mma_bf16(d, scan::bf16x2(x0.x, x0.y), scan::bf16x2(x1.x, x1.y), scan::bf16x2(x2.x, x2.y),
+                   scan::bf16x2(x3.x, x3.y), b0, b1);
+  }
+}
+
 // d += sum over k < 8 nk of A(m, k) B(k, n) on the 16 x 8 tile at (m0, n0):
 // A(m, k) = TA ? a[k lda + m] : a[m lda + k];  B(k, n) = TB ? b[n ldb + k] : b[k ldb + n].
 template <bool TA, bool TB>
@@ -188,6 +220,52 @@ __device__ void solve_unit_lower(float *AT, int lda, float *X) {
   }
 }
 
+// Row and column of element e = start + k * step of a row-major walk with
+// `cols` columns, advanced without a division per element (a runtime 64-bit
+// division costs dozens of instructions).
+struct Walk2D {
+  int r, c, dr, dc, cols;
+  __device__ __forceinline__ Walk2D(int start, int step, int cols_) : cols(cols_) {
+    r = start / cols_;
+    c = start - r * cols_;
+    dr = step / cols_;
+    dc = step - dr * cols_;
+  }
+  __device__ __forceinline__ void next() {
+    r += dr;
+    c += dc;
+    if (c >= cols) {
+      c -= cols;
+      ++r;
+    }
+  }
+};
+
+// A rows x cols fp32 tile from global memory (row stride lds) into shared
+// memory (row stride ldd), zero past rows_ok rows and cols_ok columns.  Each
+// thread has B loads in flight before it stores any, so a tile costs one or
+// two memory round trips rather than one per element a thread moves.  All 256
+// threads.
+template <int B = 8>
+__device__ __forceinline__ void tile_to_smem(float *dst, int64_t ldd, const float *__restrict__ src, int64_t lds,
+                                             int rows, int cols, int rows_ok, int cols_ok) {
+  Walk2D wk(threadIdx.x, 256, cols);
+  for (; wk.r < rows;) {
+    float v[B];
+    int rr[B], cc[B];
+#pragma unroll
+    for (int u = 0; u < B; ++u) {
+      rr[u] = wk.r;
+      cc[u] = wk.c;
+      v[u] = (wk.r < rows_ok && wk.c < cols_ok) ? src[(int64_t)wk.r * lds + wk.c] : 0.f;
+      wk.next();
+    }
+#pragma unroll
+    for (int u = 0; u < B; ++u)
+      if (rr[u] < rows) dst[(int64_t)rr[u] * ldd + cc[u]] = v[u];
+  }
+}
+
 // Rows of q (optional) and k, L2-normalized if asked, zero past Lc and past K,
 // into qs and ks (row stride xl >= kpad(K) + 4).  Four rows per warp have
 // their loads in flight before any row is reduced.  All 256 threads.
@@ -252,9 +330,9 @@ __host__ __device__ constexpr int64_t gram_scratch_floats(int C, int64_t K, bool
 // Gram tiles, then e^{G_i - G_j} per entry.  Per-key gate: diagonal 16 x 16
 // blocks entry by entry; block row a > 0 against rows 0 .. 16a-1 as one
 // product of X_i e^{G_i - G_r} and Y_j e^{G_r - G_j}, r = 16 a, so no factor
-// has a positive exponent for non-positive gates.  All 256 threads; ends
-// with a barrier.
-template <int C, bool PER_K, bool STRICT>
+// has a positive exponent for non-positive gates.  FAST takes the hardware
+// exponential (the bf16 path).  All 256 threads; ends with a barrier.
+template <int C, bool PER_K, bool STRICT, bool FAST = false>
 __device__ void decayed_gram(const float *X, const float *Y, int64_t xl, const float *gam, int64_t gl, int64_t K,
                              int Lc, const float *s, float *out, int lo, float *Xs, float *Ys) {
   constexpr int kWarps = 8;
@@ -276,7 +354,7 @@ __device__ void decayed_gram(const float *X, const float *Y, int64_t xl, const f
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = m0 + gq + 8 * (e >> 1), j = n0 + 2 * tq + (e & 1);
-        out[i * lo + j] = (below(i, j) && i < Lc) ? (s ? s[i] : 1.f) * expf(gam[i] - gam[j]) * d[e] : 0.f;
+        out[i * lo + j] = (below(i, j) && i < Lc) ? (s ? s[i] : 1.f) * scan::exp_<FAST>(gam[i] - gam[j]) * d[e] : 0.f;
       }
     }
     __syncthreads();
@@ -295,7 +373,7 @@ __device__ void decayed_gram(const float *X, const float *Y, int64_t xl, const f
     float acc = 0.f;
     if (below(i, j) && i < Lc) {
       const float *xr = X + i * xl, *yr = Y + j * xl, *gi = gam + i * gl, *gj = gam + j * gl;
-      for (int64_t d = 0; d < K; ++d) acc = fmaf(xr[d] * yr[d], expf(gi[d] - gj[d]), acc);
+      for (int64_t d = 0; d < K; ++d) acc = fmaf(xr[d] * yr[d], scan::exp_<FAST>(gi[d] - gj[d]), acc);
       acc *= s ? s[i] : 1.f;
     }
     out[i * lo + j] = acc;
@@ -303,15 +381,15 @@ __device__ void decayed_gram(const float *X, const float *Y, int64_t xl, const f
   for (int a = 1; factored && a < C / 16 && 16 * a < Lc; ++a) {
     const int r = 16 * a;
     __syncthreads();
-    for (int64_t e = tid; e < (16 + r) * Kp; e += 256) {
-      const int row = (int)(e / Kp);
-      const int64_t d = e % Kp;
+    for (Walk2D wk(tid, 256, (int)Kp); wk.r < 16 + r; wk.next()) {
+      const int row = wk.r;
+      const int64_t d = wk.c;
       if (row < 16) {
         const int i = r + row;
-        Xs[row * xl + d] = (d < K && i < Lc) ? X[i * xl + d] * expf(gam[i * gl + d] - gam[r * gl + d]) : 0.f;
+        Xs[row * xl + d] = (d < K && i < Lc) ? X[i * xl + d] * scan::exp_<FAST>(gam[i * gl + d] - gam[r * gl + d]) : 0.f;
       } else {
         const int jr = row - 16;
-        Ys[jr * xl + d] = d < K ? Y[jr * xl + d] * expf(gam[r * gl + d] - gam[jr * gl + d]) : 0.f;
+        Ys[jr * xl + d] = d < K ? Y[jr * xl + d] * scan::exp_<FAST>(gam[r * gl + d] - gam[jr * gl + d]) : 0.f;
       }
     }
     __syncthreads();

@@ -19,6 +19,8 @@
 // Pages cited: the KCP handbook = "flash-linear-attention KCP 精度失效根因排查手册".
 #pragma once
 
+#include <type_traits>
+
 #include "gdr_device.cuh"
 #include "gdr_sm100.cuh"
 
@@ -61,6 +63,35 @@ __device__ __forceinline__ void mma3(float (&d)[4], const uint32_t (&ah)[4], con
   sm100::mma_tf32(d, ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
   sm100::mma_tf32(d, ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
 }
+
+// mma.sync m16n8k16 with bf16 inputs and fp32 accumulation (one pass), for
+// products whose operands the bf16 path takes in bf16 anyway (as the fused form
+// does).  Each 32-bit register holds two bf16, the lower half the smaller K
+// index.  Fragments (g = lane / 4, t = lane % 4): A (16x16) a0 (g, 2t..2t+1)
+// a1 (g+8, 2t..) a2 (g, 2t+8..) a3 (g+8, 2t+8..); B (16x8, K x N) b0 (2t..2t+1, g)
+// b1 (2t+8.., g); D as for m16n8k8.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// two fp32 values rounded to a bf16 pair, x0 in the lower half
+__device__ __forceinline__ uint32_t bf16x2(float x0, float x1) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(x0, x1);
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+// e^x: the fast hardware exponential on the bf16 path, the full-precision one otherwise
+template <bool FAST>
+__device__ __forceinline__ float exp_(float x) {
+  return FAST ? __expf(x) : expf(x);
+}
+
+// bf16 inputs take the single-pass bf16 products and the fast exponential
+template <typename Tin>
+constexpr bool kB16 = std::is_same<Tin, __nv_bfloat16>::value;
 
 // Kb rows (L2-normalized k times e^{G_L - G}) into kt and -w into ws, for the
 // chunk's rows, zero past Lc and past K.  Warp w takes rows w, w + 8, ...; the
@@ -106,7 +137,7 @@ __device__ __forceinline__ void load_rows(const Tiles &s, const Tin *__restrict_
         const int64_t d = lane + 32 * m;
         if (d < Kp) {
           const bool ok = rok && d < K;
-          s.kt[i * KL + d] = ok ? kv[r][m] * sc * expf(s.gl[d] - gv[r][m]) : 0.f;
+          s.kt[i * KL + d] = ok ? kv[r][m] * sc * exp_<kB16<Tin>>(s.gl[d] - gv[r][m]) : 0.f;
           s.ws[i * WL + d] = ok ? -wv[r][m] : 0.f;
         }
       }
@@ -150,20 +181,36 @@ __device__ __forceinline__ void chunk_step(const Tiles &s, const Tin *__restrict
         const int64_t col = c0col + n0 + 8 * nt + 2 * tq + (e & 1);
         acc[nt][e] = (i < Lc && col < ucols) ? u[((t0 + i) * HV + hv) * V + col] : 0.f;
       }
-    for (int64_t k0 = 0; k0 < Kp; k0 += 8) {
-      uint32_t ah[4], al[4];
-      const float *a = s.ws + (m0 + g) * WL + k0 + tq;
-      split3(a[0], ah[0], al[0]);
-      split3(a[8 * WL], ah[1], al[1]);
-      split3(a[4], ah[2], al[2]);
-      split3(a[8 * WL + 4], ah[3], al[3]);
+    if constexpr (kB16<Tin>) {
+      for (int64_t k0 = 0; k0 < Kp; k0 += 16) {
+        const float *a = s.ws + (m0 + g) * WL + k0 + 2 * tq;
+        const float2 x0 = *reinterpret_cast<const float2 *>(a), x1 = *reinterpret_cast<const float2 *>(a + 8 * WL),
+                     x2 = *reinterpret_cast<const float2 *>(a + 8),
+                     x3 = *reinterpret_cast<const float2 *>(a + 8 * WL + 8);
+        const uint32_t a0 = bf16x2(x0.x, x0.y), a1 = bf16x2(x1.x, x1.y), a2 = bf16x2(x2.x, x2.y),
+                       a3 = bf16x2(x3.x, x3.y);
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const float *b = s.hs + (k0 + tq) * kHS + n0 + 8 * nt + g;
-        uint32_t bh[2], bl[2];
-        split3(b[0], bh[0], bl[0]);
-        split3(b[4 * kHS], bh[1], bl[1]);
-        mma3(acc[nt], ah, al, bh, bl);
+        for (int nt = 0; nt < 2; ++nt) {
+          const float *b = s.hs + (k0 + 2 * tq) * kHS + n0 + 8 * nt + g;
+          mma_bf16(acc[nt], a0, a1, a2, a3, bf16x2(b[0], b[kHS]), bf16x2(b[8 * kHS], b[9 * kHS]));
+        }
+      }
+    } else {
+      for (int64_t k0 = 0; k0 < Kp; k0 += 8) {
+        uint32_t ah[4], al[4];
+        const float *a = s.ws + (m0 + g) * WL + k0 + tq;
+        split3(a[0], ah[0], al[0]);
+        split3(a[8 * WL], ah[1], al[1]);
+        split3(a[4], ah[2], al[2]);
+        split3(a[8 * WL + 4], ah[3], al[3]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const float *b = s.hs + (k0 + tq) * kHS + n0 + 8 * nt + g;
+          uint32_t bh[2], bl[2];
+          split3(b[0], bh[0], bl[0]);
+          split3(b[4 * kHS], bh[1], bl[1]);
+          mma3(acc[nt], ah, al, bh, bl);
+        }
       }
     }
 #pragma unroll
@@ -182,7 +229,7 @@ __device__ __forceinline__ void chunk_step(const Tiles &s, const Tin *__restrict
   // ---- h <- e^{G_L} h + Kb^T v_new: Kp x 32, warp -> row tiles warp, warp + 8, ..., all 4 column tiles
   for (int64_t m0 = 16 * warp; m0 < Kp; m0 += 16 * kWarps) {
     float acc[4][4];
-    const float e0 = expf(s.gl[PER_K ? m0 + g : 0]), e1 = expf(s.gl[PER_K ? m0 + g + 8 : 0]);
+    const float e0 = exp_<kB16<Tin>>(s.gl[PER_K ? m0 + g : 0]), e1 = exp_<kB16<Tin>>(s.gl[PER_K ? m0 + g + 8 : 0]);
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
@@ -190,21 +237,35 @@ __device__ __forceinline__ void chunk_step(const Tiles &s, const Tin *__restrict
         const int64_t d = m0 + g + 8 * (e >> 1);
         acc[nt][e] = s.hs[d * kHS + 8 * nt + 2 * tq + (e & 1)] * ((e >> 1) ? e1 : e0);
       }
+    if constexpr (kB16<Tin>) {
 #pragma unroll
-    for (int k0 = 0; k0 < C; k0 += 8) {
-      uint32_t ah[4], al[4];
-      const float *a = s.kt + (k0 + tq) * KL + m0 + g;  // A(d, i) = Kb[i][d]
-      split3(a[0], ah[0], al[0]);
-      split3(a[8], ah[1], al[1]);
-      split3(a[4 * KL], ah[2], al[2]);
-      split3(a[4 * KL + 8], ah[3], al[3]);
+      for (int k0 = 0; k0 < C; k0 += 16) {
+        const float *a = s.kt + (k0 + 2 * tq) * KL + m0 + g;  // A(d, i) = Kb[i][d]
+        const uint32_t a0 = bf16x2(a[0], a[KL]), a1 = bf16x2(a[8], a[KL + 8]), a2 = bf16x2(a[8 * KL], a[9 * KL]),
+                       a3 = bf16x2(a[8 * KL + 8], a[9 * KL + 8]);
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const float *b = s.vn + (k0 + tq) * kHS + 8 * nt + g;
-        uint32_t bh[2], bl[2];
-        split3(b[0], bh[0], bl[0]);
-        split3(b[4 * kHS], bh[1], bl[1]);
-        mma3(acc[nt], ah, al, bh, bl);
+        for (int nt = 0; nt < 4; ++nt) {
+          const float *b = s.vn + (k0 + 2 * tq) * kHS + 8 * nt + g;
+          mma_bf16(acc[nt], a0, a1, a2, a3, bf16x2(b[0], b[kHS]), bf16x2(b[8 * kHS], b[9 * kHS]));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int k0 = 0; k0 < C; k0 += 8) {
+        uint32_t ah[4], al[4];
+        const float *a = s.kt + (k0 + tq) * KL + m0 + g;  // A(d, i) = Kb[i][d]
+        split3(a[0], ah[0], al[0]);
+        split3(a[8], ah[1], al[1]);
+        split3(a[4 * KL], ah[2], al[2]);
+        split3(a[4 * KL + 8], ah[3], al[3]);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          const float *b = s.vn + (k0 + tq) * kHS + 8 * nt + g;
+          uint32_t bh[2], bl[2];
+          split3(b[0], bh[0], bl[0]);
+          split3(b[4 * kHS], bh[1], bl[1]);
+          mma3(acc[nt], ah, al, bh, bl);
+        }
       }
     }
 #pragma unroll
