@@ -145,6 +145,85 @@ __device__ __forceinline__ void load_rows(const Tiles &s, const Tin *__restrict_
   }
 }
 
+// The same rows with vector loads, for K % 4 == 0, K <= 128 and 16-byte
+// aligned k, w and gcum: lane l takes the four keys 4l .. 4l + 3 of a row (one
+// load per row and tensor instead of four), four rows per warp in flight.
+template <typename Tin, int C, bool PER_K>
+__device__ __forceinline__ void load_rows_vec(const Tiles &s, const Tin *__restrict__ k, const float *__restrict__ w,
+                                              const float *__restrict__ gcum, int64_t t0, int Lc, int64_t hv,
+                                              int64_t hq, int64_t H, int64_t HV, int64_t K, int l2) {
+  constexpr int kWarps = kScanThreads / 32;
+  constexpr int RPW = C / kWarps, RB = 4;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t Kp = kpad(K), WL = ws_ld(K), KL = kt_ld(K);
+  const int d0 = 4 * lane;
+  const bool lane_in = d0 < K;
+#pragma unroll
+  for (int jb = 0; jb < RPW; jb += RB) {
+    float kv[RB][4], gv[RB][4], wv[RB][4];
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      const int i = warp + kWarps * (jb + r);
+      const bool ok = lane_in && i < Lc;
+      const int64_t tok = t0 + i;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) kv[r][m] = gv[r][m] = wv[r][m] = 0.f;
+      if (ok) {
+        if constexpr (kB16<Tin>) {
+          const uint2 kk = *reinterpret_cast<const uint2 *>(k + (tok * H + hq) * K + d0);
+          const float2 k01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kk.x));
+          const float2 k23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kk.y));
+          kv[r][0] = k01.x;
+          kv[r][1] = k01.y;
+          kv[r][2] = k23.x;
+          kv[r][3] = k23.y;
+        } else {
+          const float4 kk = *reinterpret_cast<const float4 *>(k + (tok * H + hq) * K + d0);
+          kv[r][0] = kk.x;
+          kv[r][1] = kk.y;
+          kv[r][2] = kk.z;
+          kv[r][3] = kk.w;
+        }
+        const float4 ww = *reinterpret_cast<const float4 *>(w + (tok * HV + hv) * K + d0);
+        wv[r][0] = ww.x;
+        wv[r][1] = ww.y;
+        wv[r][2] = ww.z;
+        wv[r][3] = ww.w;
+        if constexpr (PER_K) {
+          const float4 gg = *reinterpret_cast<const float4 *>(gcum + (tok * HV + hv) * K + d0);
+          gv[r][0] = gg.x;
+          gv[r][1] = gg.y;
+          gv[r][2] = gg.z;
+          gv[r][3] = gg.w;
+        } else {
+          gv[r][0] = gv[r][1] = gv[r][2] = gv[r][3] = gcum[tok * HV + hv];
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      if (jb + r >= RPW) break;
+      const int i = warp + kWarps * (jb + r);
+      float ss = 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) ss = fmaf(kv[r][m], kv[r][m], ss);
+      const float sc = l2 ? rsqrtf(warp_sum(ss) + kL2Eps) : 1.f;
+      if (d0 < Kp) {
+        const bool ok = lane_in && i < Lc;
+        float4 kb = make_float4(0.f, 0.f, 0.f, 0.f), nw = kb;
+        if (ok) {
+          const float4 gl = *reinterpret_cast<const float4 *>(s.gl + d0);
+          kb = make_float4(kv[r][0] * sc * exp_<kB16<Tin>>(gl.x - gv[r][0]), kv[r][1] * sc * exp_<kB16<Tin>>(gl.y - gv[r][1]),
+                           kv[r][2] * sc * exp_<kB16<Tin>>(gl.z - gv[r][2]), kv[r][3] * sc * exp_<kB16<Tin>>(gl.w - gv[r][3]));
+          nw = make_float4(-wv[r][0], -wv[r][1], -wv[r][2], -wv[r][3]);
+        }
+        *reinterpret_cast<float4 *>(s.kt + i * KL + d0) = kb;
+        *reinterpret_cast<float4 *>(s.ws + i * WL + d0) = nw;
+      }
+    }
+  }
+}
+
 // One chunk.  Called by all 256 threads of the block; hs holds the entering
 // tile and holds the leaving one on return.  v_new_out (nullable) receives
 // v_new for rows < Lc and columns < ucols.  c0col is the tile's first column
@@ -165,7 +244,11 @@ __device__ __forceinline__ void chunk_step(const Tiles &s, const Tin *__restrict
   __syncthreads();
   // Kb and -w, zero past Lc and past K
   constexpr int kWarps = kScanThreads / 32;
-  if (K <= 128) load_rows<Tin, C, PER_K, 4, 4>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
+  const bool vec = K <= 128 && K % 4 == 0 &&
+                   ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(gcum)) &
+                    15u) == 0;  // every row then starts on a 16-byte (bf16 k: 8-byte) boundary
+  if (vec) load_rows_vec<Tin, C, PER_K>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
+  else if (K <= 128) load_rows<Tin, C, PER_K, 4, 4>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
   else load_rows<Tin, C, PER_K, 8, 2>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
   __syncthreads();
 
