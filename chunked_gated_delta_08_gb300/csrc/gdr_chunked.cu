@@ -127,14 +127,14 @@ __global__ void chunk_index_kernel(const int64_t *__restrict__ cu, int64_t N, in
 //             factors have non-positive exponents (the "safe gate" reading)
 //   T       = (I + A)^-1 by blocks (prep::solve_unit_lower)
 //   w, u    = T [diag(beta e^G) K | diag(beta) V], 64-column tiles
-// smem: ks[C][KL] | gam[C][Kp] or [C] | bet[C] | AT[C][C+1] | Tm[C][C+4] |
+// smem: ks[C][KL] | gam[C][Kp + 4] or [C] | bet[C] | AT[C][C+1] | Tm[C][C+4] |
 //       Bt[C][72] | Xs[16][KL] | Ys[C][KL]   (KL = Kp + 4; Xs, Ys per-key, K <= 128)
 // --------------------------------------------------------------------------
 constexpr int kBtCols = 64;
 constexpr int kBtLd = kBtCols + 8;
 
 __host__ __device__ constexpr int64_t prep_smem_floats(int C, int64_t K, bool per_k) {
-  return C * (scan::kpad(K) + 4) + (per_k ? C * scan::kpad(K) : C) + C + C * (C + 1) + C * (C + 4) + C * kBtLd +
+  return C * (scan::kpad(K) + 4) + (per_k ? C * (scan::kpad(K) + 4) : C) + C + C * (C + 1) + C * (C + 4) + C * kBtLd +
          prep::gram_scratch_floats(C, K, per_k);
 }
 
@@ -145,11 +145,11 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(
     int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V, int l2, int beta_logits, float *__restrict__ gcum,
     float *__restrict__ w, float *__restrict__ u) {
   extern __shared__ float smem[];
-  const int64_t Kp = scan::kpad(K), KL = Kp + 4, GL = PER_K ? Kp : 1;
+  const int64_t Kp = scan::kpad(K), KL = Kp + 4, GL = PER_K ? Kp + 4 : 1;
   constexpr int LA = C + 1, LT = C + 4;
   float *ks = smem;
   float *gam = ks + C * KL;
-  float *bet = gam + (PER_K ? C * Kp : C);
+  float *bet = gam + (PER_K ? C * GL : C);
   float *AT = bet + C;
   float *Tm = AT + C * LA;
   float *Bt = Tm + C * LT;
@@ -323,7 +323,7 @@ __host__ __device__ constexpr int64_t fwd_o_ks_floats(int C, int64_t K) {
 }
 
 __host__ __device__ constexpr int64_t fwd_o_smem_floats(int C, int64_t K, bool per_k) {
-  return C * (scan::kpad(K) + 4) + fwd_o_ks_floats(C, K) + (per_k ? C * scan::kpad(K) : C) + C * (C + 4) +
+  return C * (scan::kpad(K) + 4) + fwd_o_ks_floats(C, K) + (per_k ? C * (scan::kpad(K) + 4) : C) + C * (C + 4) +
          C * kOLd + prep::gram_scratch_floats(C, K, per_k);
 }
 
@@ -334,13 +334,13 @@ __global__ void __launch_bounds__(kThreads) fwd_o_kernel(
     const int64_t *__restrict__ chunk_indices, int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V,
     int l2, Tin *__restrict__ o) {
   extern __shared__ float smem[];
-  const int64_t Kp = scan::kpad(K), KL = Kp + 4, GL = PER_K ? Kp : 1;
+  const int64_t Kp = scan::kpad(K), KL = Kp + 4, GL = PER_K ? Kp + 4 : 1;
   constexpr int LP = C + 4;
   float *qs = smem;
   float *ks = qs + C * KL;
   float *hs = ks;
   float *gam = ks + fwd_o_ks_floats(C, K);
-  float *P = gam + (PER_K ? C * Kp : C);
+  float *P = gam + (PER_K ? C * GL : C);
   float *vn = P + C * LP;
   float *Xs = vn + C * kOLd;
   float *Ys = Xs + 16 * KL;
