@@ -365,12 +365,7 @@ __global__ void __launch_bounds__(kThreads) fwd_o_kernel(
     if (d < K) qs[i * KL + d] *= scan::exp_<scan::kB16<Tin>>(PER_K ? gam[i * GL + d] : gam[i]);
   }
 
-  for (int64_t v0 = 0; v0 < V; v0 += kOCols) {
-    __syncthreads();  // q * e^G done; the previous tile's reads of hs and vn done
-    const int vok = (int)(V - v0 < kOCols ? V - v0 : kOCols);
-    prep::tile_to_smem(hs, kOLd, h + (chunk * HV + hv) * K * V + v0, V, (int)Kp, kOCols, (int)K, vok);
-    prep::tile_to_smem(vn, kOLd, v_new + (t0 * HV + hv) * V + v0, HV * V, C, kOCols, Lc, vok);
-    __syncthreads();
+  auto products = [&](int64_t v0) {
     for (int tix = warp; tix < (C / 16) * (kOCols / 8); tix += kWarps) {
       const int m0 = 16 * (tix % (C / 16)), n0 = 8 * (tix / (C / 16));
       float d1[4], d2[4];
@@ -387,6 +382,34 @@ __global__ void __launch_bounds__(kThreads) fwd_o_kernel(
         const int64_t col = v0 + n0 + 2 * tq + (e & 1);
         if (i < Lc && col < V) o[((t0 + i) * HV + hv) * V + col] = from_f32<Tin>(d1[e] + d2[e]);
       }
+    }
+  };
+  const float *hsrc = h + (chunk * HV + hv) * K * V, *vsrc = v_new + (t0 * HV + hv) * V;
+  auto vok = [&](int64_t v0) { return (int)(V - v0 < kOCols ? V - v0 : kOCols); };
+  if (Kp <= 128) {
+    // the next V tile's h and v_new rows load into registers while this tile's products run
+    prep::TileRegs<128 * kOCols / kThreads> th;
+    prep::TileRegs<C * kOCols / kThreads> tv;
+    th.get(hsrc, V, kOCols, (int)K, vok(0));
+    tv.get(vsrc, HV * V, kOCols, Lc, vok(0));
+    for (int64_t v0 = 0; v0 < V; v0 += kOCols) {
+      __syncthreads();  // q * e^G done; the previous tile's reads of hs and vn done
+      th.put(hs, kOLd, (int)Kp, kOCols);
+      tv.put(vn, kOLd, C, kOCols);
+      __syncthreads();
+      if (v0 + kOCols < V) {
+        th.get(hsrc + v0 + kOCols, V, kOCols, (int)K, vok(v0 + kOCols));
+        tv.get(vsrc + v0 + kOCols, HV * V, kOCols, Lc, vok(v0 + kOCols));
+      }
+      products(v0);
+    }
+  } else {
+    for (int64_t v0 = 0; v0 < V; v0 += kOCols) {
+      __syncthreads();  // q * e^G done; the previous tile's reads of hs and vn done
+      prep::tile_to_smem(hs, kOLd, hsrc + v0, V, (int)Kp, kOCols, (int)K, vok(v0));
+      prep::tile_to_smem(vn, kOLd, vsrc + v0, HV * V, C, kOCols, Lc, vok(v0));
+      __syncthreads();
+      products(v0);
     }
   }
 }

@@ -246,7 +246,7 @@ struct Walk2D {
 // thread has B loads in flight before it stores any, so a tile costs one or
 // two memory round trips rather than one per element a thread moves.  All 256
 // threads.
-template <int B = 8>
+template <int B = 16>
 __device__ __forceinline__ void tile_to_smem(float *dst, int64_t ldd, const float *__restrict__ src, int64_t lds,
                                              int rows, int cols, int rows_ok, int cols_ok) {
   Walk2D wk(threadIdx.x, 256, cols);
@@ -265,6 +265,30 @@ __device__ __forceinline__ void tile_to_smem(float *dst, int64_t ldd, const floa
       if (rr[u] < rows) dst[(int64_t)rr[u] * ldd + cc[u]] = v[u];
   }
 }
+
+// A tile like tile_to_smem's held in registers between its loads and its
+// stores (N elements per thread, N * 256 >= rows * cols), so the loads of the
+// next tile can be in flight while the current one is used.
+template <int N>
+struct TileRegs {
+  float v[N];
+  __device__ __forceinline__ void get(const float *__restrict__ src, int64_t lds, int cols, int rows_ok, int cols_ok) {
+    Walk2D wk(threadIdx.x, 256, cols);
+#pragma unroll
+    for (int u = 0; u < N; ++u) {
+      v[u] = (wk.r < rows_ok && wk.c < cols_ok) ? src[(int64_t)wk.r * lds + wk.c] : 0.f;
+      wk.next();
+    }
+  }
+  __device__ __forceinline__ void put(float *dst, int64_t ldd, int rows, int cols) const {
+    Walk2D wk(threadIdx.x, 256, cols);
+#pragma unroll
+    for (int u = 0; u < N; ++u) {
+      if (wk.r < rows) dst[(int64_t)wk.r * ldd + wk.c] = v[u];
+      wk.next();
+    }
+  }
+};
 
 // Rows of q (optional) and k, L2-normalized if asked, zero past Lc and past K,
 // into qs and ks (row stride xl >= kpad(K) + 4).  Four rows per warp have
