@@ -62,7 +62,9 @@ typedef enum gdr_dtype { GDR_F32 = 0, GDR_BF16 = 1 } gdr_dtype;
 typedef enum gdr_gate { GDR_GATE_SCALAR = 0, GDR_GATE_PER_K = 1 } gdr_gate;
 typedef enum gdr_algo {
   GDR_ALGO_AUTO = 0,     /* fused single pass where supported, else the chunked three-kernel form */
-  GDR_ALGO_CHUNKED = 1,  /* chunk index -> prepare -> fwd_h -> fwd_o, fp32 CUDA-core arithmetic */
+  GDR_ALGO_CHUNKED = 1,  /* chunk index -> prepare -> fwd_h -> fwd_o; warp-level tensor-core products in
+                            3 x TF32 for fp32 inputs; for bf16 inputs the Gram matrices and the solve in
+                            3 x TF32, the other products in one bf16 pass (fp32 accumulation) */
   GDR_ALGO_FUSED = 2,    /* one persistent pass per (sequence, value head), tcgen05 tensor cores */
   GDR_ALGO_RECURRENT = 3, /* token by token, state in registers (decode and other short inputs) */
   GDR_ALGO_SPLIT = 4      /* chunked, state scan split into 1024-token segments merged by transitions */
