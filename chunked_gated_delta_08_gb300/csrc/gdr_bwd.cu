@@ -84,7 +84,7 @@ __device__ __forceinline__ void load_gamma(const float *__restrict__ gcum, int64
 constexpr int kDvLd = 40;
 
 __host__ __device__ constexpr int64_t dv_local_smem_floats(int C, int64_t K, bool per_k) {
-  return 2 * C * (scan::kpad(K) + 4) + (per_k ? C * scan::kpad(K) : C) + C * (C + 4) + C * kDvLd +
+  return 2 * C * (scan::kpad(K) + 4) + (per_k ? C * (scan::kpad(K) + 4) : C) + C * (C + 4) + C * kDvLd +
          prep::gram_scratch_floats(C, K, per_k);
 }
 
@@ -94,12 +94,12 @@ __global__ void __launch_bounds__(kThreads) bwd_dv_local_kernel(
     const float *__restrict__ gcum, const int64_t *__restrict__ cu, const int64_t *__restrict__ chunk_indices,
     int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V, int l2, float *__restrict__ dvn) {
   extern __shared__ float smem[];
-  const int64_t Kp = scan::kpad(K), KL = Kp + 4, GL = PER_K ? Kp : 1;
+  const int64_t Kp = scan::kpad(K), KL = Kp + 4, GL = PER_K ? Kp + 4 : 1;
   constexpr int LP = C + 4;
   float *qs = smem;
   float *ks = qs + C * KL;
   float *gam = ks + C * KL;
-  float *P = gam + (PER_K ? C * Kp : C);
+  float *P = gam + (PER_K ? C * GL : C);
   float *dos = P + C * LP;
   float *Xs = dos + C * kDvLd;
   float *Ys = Xs + 16 * KL;
@@ -113,20 +113,15 @@ __global__ void __launch_bounds__(kThreads) bwd_dv_local_kernel(
   const int64_t gw = PER_K ? K : 1;
 
   prep::load_qk_rows<Tin, C>(q, k, t0, Lc, H, hq, K, l2, qs, ks, KL);
-  for (int64_t e = tid; e < C * gw; e += kThreads) {
-    const int64_t i = e / gw, d = e % gw;
-    gam[i * GL + d] = i < Lc ? gcum[((t0 + i) * HV + hv) * gw + d] : 0.f;
-  }
+  prep::tile_to_smem(gam, GL, gcum + (t0 * HV + hv) * gw, HV * gw, C, (int)gw, Lc, (int)gw);
   for (int e = tid; e < C * LP; e += kThreads) P[e] = 0.f;  // P^T reads the upper part
   __syncthreads();
   // P_ri = sum_d q_rd k_id exp(G_rd - G_id), i <= r < Lc
-  prep::decayed_gram<C, PER_K, false>(qs, ks, KL, gam, GL, K, Lc, nullptr, P, LP, Xs, Ys);
+  prep::decayed_gram<C, PER_K, false, scan::kB16<Tin>>(qs, ks, KL, gam, GL, K, Lc, nullptr, P, LP, Xs, Ys);
   for (int64_t v0 = 0; v0 < V; v0 += 32) {
     __syncthreads();
-    for (int e = tid; e < C * 32; e += kThreads) {
-      const int r = e / 32, vv = e % 32;
-      dos[r * kDvLd + vv] = (r < Lc && v0 + vv < V) ? to_f32(d_o[((t0 + r) * HV + hv) * V + v0 + vv]) : 0.f;
-    }
+    prep::tile_to_smem(dos, kDvLd, d_o + (t0 * HV + hv) * V + v0, HV * V, C, 32, Lc,
+                       (int)(V - v0 < 32 ? V - v0 : 32));
     __syncthreads();
     for (int tix = warp; tix < (C / 16) * 4; tix += kWarps) {
       const int m0 = 16 * (tix % (C / 16)), n0 = 8 * (tix / (C / 16));
@@ -190,8 +185,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dh_kernel(
       st.gl[d] = d < K ? gcum[(tl * HV + hv) * gw + (PER_K ? d : 0)] : 0.f;
     __syncthreads();
     // Kb into kt, -w into ws
-    if (K <= 128) scan::load_rows<Tin, C, PER_K, 4, 4>(st, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
-    else scan::load_rows<Tin, C, PER_K, 8, 2>(st, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
+    scan::load_rows_auto<Tin, C, PER_K>(st, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
     __syncthreads();
     // dv_new += Kb dh'
     for (int tix = warp; tix < (C / 16) * 4; tix += kWarps) {
@@ -215,22 +209,31 @@ __global__ void __launch_bounds__(kThreads) bwd_dh_kernel(
     __syncthreads();
     // Qt into kt (over Kb), do into dos
     prep::load_qk_rows<Tin, C>(nullptr, q, t0, Lc, H, hq, K, l2, nullptr, st.kt, KL);
-    for (int e = tid; e < C * kBVd; e += kThreads) {
-      const int i = e / kBVd, vv = e % kBVd;
-      dos[i * LD + vv] = (i < Lc && v0 + vv < V) ? to_f32(d_o[((t0 + i) * HV + hv) * V + v0 + vv]) : 0.f;
-    }
+    prep::tile_to_smem(dos, LD, d_o + (t0 * HV + hv) * V + v0, HV * V, C, kBVd, Lc,
+                       (int)(V - v0 < kBVd ? V - v0 : kBVd));
     __syncthreads();
-    for (int64_t e = tid; e < C * Kp; e += kThreads) {
-      const int i = (int)(e / Kp);
-      const int64_t d = e % Kp;
-      if (i < Lc && d < K) st.kt[i * KL + d] *= expf(gcum[((t0 + i) * HV + hv) * gw + (PER_K ? d : 0)]);
+    // Qt = q e^G: sixteen gate loads per thread in flight at a time
+    for (prep::Walk2D wk(tid, kThreads, (int)Kp); wk.r < C;) {
+      float gv[16];
+      int rr[16], cc[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        rr[u] = wk.r;
+        cc[u] = wk.c;
+        gv[u] = (wk.r < Lc && wk.c < K) ? gcum[((t0 + wk.r) * HV + hv) * gw + (PER_K ? wk.c : 0)] : 0.f;
+        wk.next();
+      }
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        if (rr[u] < Lc && cc[u] < K) st.kt[rr[u] * KL + cc[u]] *= scan::exp_<scan::kB16<Tin>>(gv[u]);
     }
     __syncthreads();
     // dh = e^{G_L} dh' + Qt^T do - w^T dv_new
     for (int tix = warp; tix < (int)(Kp / 16) * 4; tix += kWarps) {
       const int m0 = 16 * (tix % (int)(Kp / 16)), n0 = 8 * (tix / (int)(Kp / 16));
       float d[4];
-      const float e0 = expf(st.gl[PER_K ? m0 + gq : 0]), e1 = expf(st.gl[PER_K ? m0 + gq + 8 : 0]);
+      const float e0 = scan::exp_<scan::kB16<Tin>>(st.gl[PER_K ? m0 + gq : 0]),
+                  e1 = scan::exp_<scan::kB16<Tin>>(st.gl[PER_K ? m0 + gq + 8 : 0]);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int r = m0 + gq + 8 * (e >> 1), cc = n0 + 2 * tq + (e & 1);

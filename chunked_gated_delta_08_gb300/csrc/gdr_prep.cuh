@@ -241,13 +241,13 @@ struct Walk2D {
   }
 };
 
-// A rows x cols fp32 tile from global memory (row stride lds) into shared
-// memory (row stride ldd), zero past rows_ok rows and cols_ok columns.  Each
+// A rows x cols tile from global memory (row stride lds; fp32 or bf16,
+// widened to fp32) into shared memory (row stride ldd), zero past rows_ok rows and cols_ok columns.  Each
 // thread has B loads in flight before it stores any, so a tile costs one or
 // two memory round trips rather than one per element a thread moves.  All 256
 // threads.
-template <int B = 16>
-__device__ __forceinline__ void tile_to_smem(float *dst, int64_t ldd, const float *__restrict__ src, int64_t lds,
+template <int B = 16, typename Ts = float>
+__device__ __forceinline__ void tile_to_smem(float *dst, int64_t ldd, const Ts *__restrict__ src, int64_t lds,
                                              int rows, int cols, int rows_ok, int cols_ok) {
   Walk2D wk(threadIdx.x, 256, cols);
   for (; wk.r < rows;) {
@@ -257,7 +257,7 @@ __device__ __forceinline__ void tile_to_smem(float *dst, int64_t ldd, const floa
     for (int u = 0; u < B; ++u) {
       rr[u] = wk.r;
       cc[u] = wk.c;
-      v[u] = (wk.r < rows_ok && wk.c < cols_ok) ? src[(int64_t)wk.r * lds + wk.c] : 0.f;
+      v[u] = (wk.r < rows_ok && wk.c < cols_ok) ? to_f32(src[(int64_t)wk.r * lds + wk.c]) : 0.f;
       wk.next();
     }
 #pragma unroll

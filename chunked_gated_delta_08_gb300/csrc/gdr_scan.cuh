@@ -224,6 +224,21 @@ __device__ __forceinline__ void load_rows_vec(const Tiles &s, const Tin *__restr
   }
 }
 
+// The row loader for the shape: vector loads where K % 4 == 0, K <= 128 and
+// k, w, gcum are 16-byte aligned (every row then starts on a 16-byte, bf16 k
+// an 8-byte, boundary), else the scalar loaders.
+template <typename Tin, int C, bool PER_K>
+__device__ __forceinline__ void load_rows_auto(const Tiles &s, const Tin *__restrict__ k, const float *__restrict__ w,
+                                               const float *__restrict__ gcum, int64_t t0, int Lc, int64_t hv,
+                                               int64_t hq, int64_t H, int64_t HV, int64_t K, int l2) {
+  const bool vec = K <= 128 && K % 4 == 0 &&
+                   ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(gcum)) &
+                    15u) == 0;
+  if (vec) load_rows_vec<Tin, C, PER_K>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
+  else if (K <= 128) load_rows<Tin, C, PER_K, 4, 4>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
+  else load_rows<Tin, C, PER_K, 8, 2>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
+}
+
 // One chunk.  Called by all 256 threads of the block; hs holds the entering
 // tile and holds the leaving one on return.  v_new_out (nullable) receives
 // v_new for rows < Lc and columns < ucols.  c0col is the tile's first column
@@ -244,12 +259,7 @@ __device__ __forceinline__ void chunk_step(const Tiles &s, const Tin *__restrict
   __syncthreads();
   // Kb and -w, zero past Lc and past K
   constexpr int kWarps = kScanThreads / 32;
-  const bool vec = K <= 128 && K % 4 == 0 &&
-                   ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(gcum)) &
-                    15u) == 0;  // every row then starts on a 16-byte (bf16 k: 8-byte) boundary
-  if (vec) load_rows_vec<Tin, C, PER_K>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
-  else if (K <= 128) load_rows<Tin, C, PER_K, 4, 4>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
-  else load_rows<Tin, C, PER_K, 8, 2>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
+  load_rows_auto<Tin, C, PER_K>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
   __syncthreads();
 
   // ---- v_new = u - w h: C x 32, warp -> rows 16 (warp & 3) .., columns 16 (warp >> 2) ..
