@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dh_kernel(
 }
 
 // --------------------------------------------------------------------------
-// dqkg: grid (nt_max, HV).  Accumulates dQt = do h^T, dW = -dv_new h^T,
+// dqkg: grid (nt_max, HV).  Accumulates dQt = do h^T, dW = -dv_new h^T (as dv_new h^T, negated when written),
 // dKb = v_new dh'^T, dP = do v_new^T over 32-column V tiles on tensor cores
 // (3 x TF32, accumulators in registers), then forms the chunk's dq^, dk^ and
 // dGamma from the output and state terms on CUDA cores, where thread t owns
@@ -321,7 +321,8 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
   const int m0 = 16 * (warp % MT);
 
   prep::load_qk_rows<Tin, C>(q, k, t0, Lc, H, hq, K, l2, qs, ks, KQ);
-  load_gamma<PER_K>(gcum, t0, Lc, C, HV, hv, K, gam, tid);
+  prep::tile_to_smem(gam, PER_K ? K : 1, gcum + (t0 * HV + hv) * (PER_K ? K : 1), HV * (PER_K ? K : 1), C,
+                     PER_K ? (int)K : 1, Lc, PER_K ? (int)K : 1);
   for (int e = tid; e < 2 * kKmax; e += kThreads) colsum[e] = 0.f;
 
   float aQ[MQ], aK[MQ];
@@ -338,20 +339,15 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
 
   for (int64_t v0 = 0; v0 < V; v0 += 32) {
     __syncthreads();  // the previous tile's reads are done
-    for (int e = tid; e < C * 32; e += kThreads) {
-      const int r = e / 32, vv = e % 32;
-      const bool ok = r < Lc && v0 + vv < V;
-      const int64_t g = ((t0 + r) * HV + hv) * V + v0 + vv;
-      doA[r * kQL + vv] = ok ? to_f32(d_o[g]) : 0.f;
-      dvA[r * kQL + vv] = ok ? -dvn[g] : 0.f;
-      vnA[r * kQL + vv] = ok ? v_new[g] : 0.f;
-    }
-    for (int64_t e = tid; e < Kp * 32; e += kThreads) {
-      const int64_t dd = e / 32, vv = e % 32;
-      const bool ok = dd < K && v0 + vv < V;
-      const int64_t g = ((chunk * HV + hv) * K + dd) * V + v0 + vv;
-      hB[dd * kQL + vv] = ok ? h[g] : 0.f;
-      dhB[dd * kQL + vv] = ok ? dhc[g] : 0.f;
+    {
+      // dvA holds +dv_new (dW = -dv_new h^T takes the sign when written)
+      const int vok = (int)(V - v0 < 32 ? V - v0 : 32);
+      const int64_t rs = (t0 * HV + hv) * V + v0, hs0 = (chunk * HV + hv) * K * V + v0;
+      prep::tile_to_smem(doA, kQL, d_o + rs, HV * V, C, 32, Lc, vok);
+      prep::tile_to_smem(dvA, kQL, dvn + rs, HV * V, C, 32, Lc, vok);
+      prep::tile_to_smem(vnA, kQL, v_new + rs, HV * V, C, 32, Lc, vok);
+      prep::tile_to_smem(hB, kQL, h + hs0, V, (int)Kp, 32, (int)K, vok);
+      prep::tile_to_smem(dhB, kQL, dhc + hs0, V, (int)Kp, 32, (int)K, vok);
     }
     __syncthreads();
     if (tid < K)
@@ -408,7 +404,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
       const int i = m0 + gq + 8 * (e >> 1), dd = n0 + 2 * tq + (e & 1);
       sQ[i * Kp + dd] = fQ[s][e];
       sK[i * Kp + dd] = fK[s][e];
-      if (i < Lc && dd < K) dW[((t0 + i) * HV + hv) * K + dd] = fW[s][e];
+      if (i < Lc && dd < K) dW[((t0 + i) * HV + hv) * K + dd] = -fW[s][e];
     }
   }
 #pragma unroll
@@ -418,7 +414,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
     for (int e = 0; e < 4; ++e) {
       const int r = m0 + gq + 8 * (e >> 1), i = n0 + 2 * tq + (e & 1);
       float val = 0.f;
-      if (r < Lc && i <= r) val = PER_K ? fP[s][e] : fP[s][e] * expf(gam[r] - gam[i]);
+      if (r < Lc && i <= r) val = PER_K ? fP[s][e] : fP[s][e] * scan::exp_<scan::kB16<Tin>>(gam[r] - gam[i]);
       dPs[r * LP + i] = val;
     }
   }
@@ -431,7 +427,8 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
   }
   __syncthreads();  // the staging is dead
   // sq = sum_{j <= i} dP_ij k_j e^{G_i - G_j} (lo), sk = sum_{r >= i} dP_ri q_r e^{G_r - G_i} (up)
-  prep::decayed_apply<C, PER_K, false>(dPs, LP, ks, qs, KQ, gam, PER_K ? K : 1, K, Lc, lo, up, Kp, Xs, Ys);
+  prep::decayed_apply<C, PER_K, false, scan::kB16<Tin>>(dPs, LP, ks, qs, KQ, gam, PER_K ? K : 1, K, Lc, lo, up, Kp,
+                                                        Xs, Ys);
 
   // dW out; dP staged (GDN folds its decay in); column sums of dKb * Kb,
   // each thread's half in a fixed slot so the sum's order is fixed
@@ -442,7 +439,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
       const int i = 2 * m + i_base;
       if (i < Lc) {
         const float gi = gam_at<PER_K>(gam, i, d, K), gL = gam_at<PER_K>(gam, Lc - 1, d, K);
-        cs = fmaf(aK[m], ks[i * KQ + d] * expf(gL - gi), cs);
+        cs = fmaf(aK[m], ks[i * KQ + d] * scan::exp_<scan::kB16<Tin>>(gL - gi), cs);
       }
     }
     colsum[i_base * kKmax + d] = cs;
@@ -456,7 +453,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
       const int i = 2 * m + i_base;
       if (i >= Lc) continue;
       const float gi = gam_at<PER_K>(gam, i, d, K), gL = gam_at<PER_K>(gam, Lc - 1, d, K);
-      const float eG = expf(gi), eL = expf(gL - gi);
+      const float eG = scan::exp_<scan::kB16<Tin>>(gi), eL = scan::exp_<scan::kB16<Tin>>(gL - gi);
       const float qv = qs[i * KQ + d], kv = ks[i * KQ + d];
       float dq = aQ[m] * eG, dk = aK[m] * eL;
       float dgm = aQ[m] * qv * eG - aK[m] * kv * eL;
@@ -464,7 +461,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
       dq += sq;
       dk += sk;
       dgm += qv * sq - kv * sk;
-      if (i == Lc - 1) dgm += (colsum[d] + colsum[kKmax + d]) + expf(gL) * gLs[d];
+      if (i == Lc - 1) dgm += (colsum[d] + colsum[kKmax + d]) + scan::exp_<scan::kB16<Tin>>(gL) * gLs[d];
       const int64_t row = (t0 + i) * HV + hv;
       dqa[row * K + d] = dq;
       dka[row * K + d] = dk;
@@ -511,7 +508,7 @@ __host__ __device__ constexpr int64_t wy_scratch_floats(int C, int64_t K, bool p
 
 __host__ __device__ constexpr int64_t wy_smem_floats(int C, int64_t K, bool per_k) {
   const int64_t KL = scan::kpad(K) + 4;
-  return C * KL + (per_k ? C * scan::kpad(K) : C) + 3 * C + C * (C + 1) + C * (C + 4) + C * (C + 1) + 2 * C * KL +
+  return C * KL + (per_k ? C * (scan::kpad(K) + 4) : C) + 3 * C + C * (C + 1) + C * (C + 4) + C * (C + 1) + 2 * C * KL +
          wy_scratch_floats(C, K, per_k);
 }
 
@@ -528,10 +525,10 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
   constexpr int MT = C / 16;
   constexpr int NAW = MT * (C / 8) / 8;  // dA tiles per warp
   extern __shared__ float smem[];
-  const int64_t Kp = scan::kpad(K), KL = Kp + 4, GL = PER_K ? Kp : 1;
+  const int64_t Kp = scan::kpad(K), KL = Kp + 4, GL = PER_K ? Kp + 4 : 1;
   float *ks = smem;
   float *gam = ks + C * KL;
-  float *bet = gam + (PER_K ? C * Kp : C);
+  float *bet = gam + (PER_K ? C * GL : C);
   float *dbs = bet + C;
   float *rowacc = dbs + C;
   float *AT = rowacc + C;
@@ -557,10 +554,7 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
   const int m0 = 16 * (warp % MT);
 
   prep::load_qk_rows<Tin, C>(nullptr, k, t0, Lc, H, hq, K, l2, nullptr, ks, KL);
-  for (int64_t e = tid; e < C * gw; e += kThreads) {
-    const int64_t i = e / gw, dd = e % gw;
-    gam[i * GL + dd] = i < Lc ? gcum[((t0 + i) * HV + hv) * gw + dd] : 0.f;
-  }
+  prep::tile_to_smem(gam, GL, gcum + (t0 * HV + hv) * gw, HV * gw, C, (int)gw, Lc, (int)gw);
   for (int i = tid; i < C; i += kThreads) {
     bet[i] = i < Lc ? load_beta(beta, (t0 + i) * HV + hv, beta_logits) : 0.f;
     dbs[i] = 0.f;
@@ -568,7 +562,7 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
   }
   __syncthreads();
   // Bm_ij = sum_d k_id k_jd e^{G_id - G_jd} (i > j); A = diag(beta) Bm
-  prep::decayed_gram<C, PER_K, true>(ks, ks, KL, gam, GL, K, Lc, nullptr, Bm, LA, Xs, Ys);
+  prep::decayed_gram<C, PER_K, true, scan::kB16<Tin>>(ks, ks, KL, gam, GL, K, Lc, nullptr, Bm, LA, Xs, Ys);
   for (int e = tid; e < C * C; e += kThreads) {
     const int i = e / C, j = e % C;
     if (j < i) AT[i * LA + j] = bet[i] * Bm[i * LA + j];
@@ -589,11 +583,10 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
   // u-path: dX = T^T dv_new per tile; dv; dbeta += rowsum(dX V); acc += dX u^T
   for (int64_t v0 = 0; v0 < V; v0 += kWt) {
     __syncthreads();
-    for (int e = tid; e < C * kWt; e += kThreads) {
-      const int j = e / kWt, c = e % kWt;
-      const bool ok = j < Lc && v0 + c < V;
-      dvt[j * kLdB + c] = ok ? dvn[((t0 + j) * HV + hv) * V + v0 + c] : 0.f;
-      ut[j * kLdA + c] = ok ? u[((t0 + j) * HV + hv) * V + v0 + c] : 0.f;
+    {
+      const int vok = (int)(V - v0 < kWt ? V - v0 : kWt);
+      prep::tile_to_smem(dvt, kLdB, dvn + (t0 * HV + hv) * V + v0, HV * V, C, kWt, Lc, vok);
+      prep::tile_to_smem(ut, kLdA, u + (t0 * HV + hv) * V + v0, HV * V, C, kWt, Lc, vok);
     }
     __syncthreads();
     for (int tix = warp; tix < MT * (kWt / 8); tix += kWarps) {
@@ -624,10 +617,8 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
   // w-path: dY = T^T dW into sY, then acc += dY w^T
   for (int64_t d0 = 0; d0 < Kp; d0 += kWt) {
     __syncthreads();
-    for (int e = tid; e < C * kWt; e += kThreads) {
-      const int j = e / kWt, c = e % kWt;
-      dwt[j * kLdB + c] = (j < Lc && d0 + c < K) ? dW[((t0 + j) * HV + hv) * K + d0 + c] : 0.f;
-    }
+    prep::tile_to_smem(dwt, kLdB, dW + (t0 * HV + hv) * K + d0, HV * K, C, kWt, Lc,
+                       (int)(K - d0 < kWt ? (K - d0 > 0 ? K - d0 : 0) : kWt));
     __syncthreads();
     for (int tix = warp; tix < MT * (kWt / 8); tix += kWarps) {
       const int mm = 16 * (tix % MT), n0 = 8 * (tix / MT);
@@ -641,11 +632,7 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
     }
   }
   __syncthreads();
-  for (int64_t e = tid; e < C * Kp; e += kThreads) {
-    const int j = (int)(e / Kp);
-    const int64_t dd = e % Kp;
-    wf[j * KL + dd] = (j < Lc && dd < K) ? w[((t0 + j) * HV + hv) * K + dd] : 0.f;
-  }
+  prep::tile_to_smem(wf, KL, w + (t0 * HV + hv) * K, HV * K, C, (int)Kp, Lc, (int)K);
   __syncthreads();
 #pragma unroll
   for (int s2 = 0; s2 < NAW; ++s2) {
@@ -668,7 +655,7 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
     float sacc = 0.f;
     for (int j = lane; j < i; j += 32) sacc = fmaf(dAs[i * LA + j], Bm[i * LA + j], sacc);
     for (int64_t dd = lane; dd < K; dd += 32)
-      sacc = fmaf(sY[i * KL + dd], ks[i * KL + dd] * expf(PER_K ? gam[i * GL + dd] : gam[i]), sacc);
+      sacc = fmaf(sY[i * KL + dd], ks[i * KL + dd] * scan::exp_<scan::kB16<Tin>>(PER_K ? gam[i * GL + dd] : gam[i]), sacc);
     sacc = warp_sum(sacc);
     if (lane == 0) dbs[i] += sacc;
   }
@@ -676,7 +663,7 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
   // dB = beta_i dA (the scalar gate folds e^{G_i - G_j} in)
   for (int e = tid; e < C * C; e += kThreads) {
     const int i = e / C, j = e % C;
-    if (j < i && i < Lc) dAs[i * LA + j] *= bet[i] * (PER_K ? 1.f : expf(gam[i] - gam[j]));
+    if (j < i && i < Lc) dAs[i * LA + j] *= bet[i] * (PER_K ? 1.f : scan::exp_<scan::kB16<Tin>>(gam[i] - gam[j]));
   }
   __syncthreads();
 
@@ -687,14 +674,15 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
   for (int m = 0; m < MQ; ++m) yv[m] = d < K ? sY[(2 * m + i_base) * KL + d] : 0.f;
   __syncthreads();
   float *lo = sY;
-  prep::decayed_apply<C, PER_K, true>(dAs, LA, ks, ks, KL, gam, GL, K, Lc, lo, up, KL, scr, scr + 16 * KL);
+  prep::decayed_apply<C, PER_K, true, scan::kB16<Tin>>(dAs, LA, ks, ks, KL, gam, GL, K, Lc, lo, up, KL, scr,
+                                                       scr + 16 * KL);
   if (d < K) {
 #pragma unroll
     for (int m = 0; m < MQ; ++m) {
       const int i = 2 * m + i_base;
       if (i >= Lc) continue;
       const float gi = PER_K ? gam[i * GL + d] : gam[i];
-      const float eG = expf(gi), kv = ks[i * KL + d], y = yv[m];
+      const float eG = scan::exp_<scan::kB16<Tin>>(gi), kv = ks[i * KL + d], y = yv[m];
       float dk = bet[i] * y * eG;
       float dgm = dk * kv;
       const float t1 = lo[i * KL + d], t2 = up[i * KL + d];

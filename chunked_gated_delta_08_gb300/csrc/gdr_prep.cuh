@@ -457,8 +457,9 @@ __device__ void decayed_gram(const float *X, const float *Y, int64_t xl, const f
 //   lo[i] += e^{G_i - G_r0} (M[i, :r0] (Y_j e^{G_r0 - G_j}))        i in block a
 //   up[i] += e^{G_r0 - G_i} (M[block a, i]^T (Y_r e^{G_r - G_r0}))  i < r0
 // where every exponent is non-positive for non-positive gates.  Xs, Ys:
-// scratch of gram_scratch_floats.  All 256 threads; ends with a barrier.
-template <int C, bool PER_K, bool STRICT>
+// scratch of gram_scratch_floats.  FAST takes the hardware exponential (bf16
+// inputs).  All 256 threads; ends with a barrier.
+template <int C, bool PER_K, bool STRICT, bool FAST = false>
 __device__ void decayed_apply(const float *M, int lm, const float *Ylo, const float *Yup, int64_t yl, const float *gam,
                               int64_t gl, int64_t K, int Lc, float *lo, float *up, int64_t lw, float *Xs, float *Ys) {
   constexpr int kWarps = 8;
@@ -484,15 +485,15 @@ __device__ void decayed_apply(const float *M, int lm, const float *Ylo, const fl
   } else {
   if (!gram_factored(K)) {  // per-key gate past K = 128: every term directly
     {
-      for (int64_t e = tid; e < C * Kp; e += 256) {
-        const int i = (int)(e / Kp);
-        const int64_t d = e % Kp;
+      for (Walk2D wk(tid, 256, (int)Kp); wk.r < C; wk.next()) {
+        const int i = wk.r;
+        const int64_t d = wk.c;
         float a = 0.f, b = 0.f;
         if (d < K && i < Lc) {
           const float gi = gam[i * gl + d];
           for (int j = 0; j < Lc; ++j) {
-            if (STRICT ? j < i : j <= i) a = fmaf(M[i * lm + j] * Ylo[j * yl + d], expf(gi - gam[j * gl + d]), a);
-            if (STRICT ? j > i : j >= i) b = fmaf(M[j * lm + i] * Yup[j * yl + d], expf(gam[j * gl + d] - gi), b);
+            if (STRICT ? j < i : j <= i) a = fmaf(M[i * lm + j] * Ylo[j * yl + d], scan::exp_<FAST>(gi - gam[j * gl + d]), a);
+            if (STRICT ? j > i : j >= i) b = fmaf(M[j * lm + i] * Yup[j * yl + d], scan::exp_<FAST>(gam[j * gl + d] - gi), b);
           }
         }
         lo[i * lw + d] = a;
@@ -503,16 +504,16 @@ __device__ void decayed_apply(const float *M, int lm, const float *Ylo, const fl
     return;
   }
   // diagonal blocks, term by term
-  for (int64_t e = tid; e < C * Kp; e += 256) {
-    const int i = (int)(e / Kp);
-    const int64_t d = e % Kp;
+  for (Walk2D wk(tid, 256, (int)Kp); wk.r < C; wk.next()) {
+    const int i = wk.r;
+    const int64_t d = wk.c;
     float a = 0.f, b = 0.f;
     if (d < K && i < Lc) {
       const int base = 16 * (i / 16), end = base + 16 < Lc ? base + 16 : Lc;
       const float gi = gam[i * gl + d];
       for (int j = base; j < end; ++j) {
-        if (STRICT ? j < i : j <= i) a = fmaf(M[i * lm + j] * Ylo[j * yl + d], expf(gi - gam[j * gl + d]), a);
-        if (STRICT ? j > i : j >= i) b = fmaf(M[j * lm + i] * Yup[j * yl + d], expf(gam[j * gl + d] - gi), b);
+        if (STRICT ? j < i : j <= i) a = fmaf(M[i * lm + j] * Ylo[j * yl + d], scan::exp_<FAST>(gi - gam[j * gl + d]), a);
+        if (STRICT ? j > i : j >= i) b = fmaf(M[j * lm + i] * Yup[j * yl + d], scan::exp_<FAST>(gam[j * gl + d] - gi), b);
       }
     }
     lo[i * lw + d] = a;
@@ -521,15 +522,15 @@ __device__ void decayed_apply(const float *M, int lm, const float *Ylo, const fl
   for (int a = 1; a < C / 16 && 16 * a < Lc; ++a) {
     const int r0 = 16 * a;
     __syncthreads();
-    for (int64_t e = tid; e < (16 + r0) * Kp; e += 256) {
-      const int row = (int)(e / Kp);
-      const int64_t d = e % Kp;
+    for (Walk2D wk(tid, 256, (int)Kp); wk.r < 16 + r0; wk.next()) {
+      const int row = wk.r;
+      const int64_t d = wk.c;
       if (row < 16) {  // Y_r e^{G_r - G_r0}, r in block a (zero past Lc)
         const int r = r0 + row;
-        Xs[row * yl + d] = (d < K && r < Lc) ? Yup[r * yl + d] * expf(gam[r * gl + d] - gam[r0 * gl + d]) : 0.f;
+        Xs[row * yl + d] = (d < K && r < Lc) ? Yup[r * yl + d] * scan::exp_<FAST>(gam[r * gl + d] - gam[r0 * gl + d]) : 0.f;
       } else {  // Y_j e^{G_r0 - G_j}, j < r0
         const int j = row - 16;
-        Ys[j * yl + d] = d < K ? Ylo[j * yl + d] * expf(gam[r0 * gl + d] - gam[j * gl + d]) : 0.f;
+        Ys[j * yl + d] = d < K ? Ylo[j * yl + d] * scan::exp_<FAST>(gam[r0 * gl + d] - gam[j * gl + d]) : 0.f;
       }
     }
     __syncthreads();
@@ -540,7 +541,7 @@ __device__ void decayed_apply(const float *M, int lm, const float *Ylo, const fl
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = r0 + gq + 8 * (e >> 1), d = 8 * nt + 2 * tq + (e & 1);
-        if (d < K && i < Lc) lo[i * lw + d] += acc[e] * expf(gam[i * gl + d] - gam[r0 * gl + d]);
+        if (d < K && i < Lc) lo[i * lw + d] += acc[e] * scan::exp_<FAST>(gam[i * gl + d] - gam[r0 * gl + d]);
       }
     }
     // up rows 0 .. r0-1: M[block a, :r0]^T Xs, scaled by e^{G_r0 - G_i}
@@ -551,7 +552,7 @@ __device__ void decayed_apply(const float *M, int lm, const float *Ylo, const fl
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = m0 + gq + 8 * (e >> 1), d = n0 + 2 * tq + (e & 1);
-        if (d < K && i < Lc) up[i * lw + d] += acc[e] * expf(gam[r0 * gl + d] - gam[i * gl + d]);
+        if (d < K && i < Lc) up[i * lw + d] += acc[e] * scan::exp_<FAST>(gam[r0 * gl + d] - gam[i * gl + d]);
       }
     }
   }
