@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dv_local_kernel(
     for (int tix = warp; tix < (C / 16) * 4; tix += kWarps) {
       const int m0 = 16 * (tix % (C / 16)), n0 = 8 * (tix / (C / 16));
       float d[4] = {0.f, 0.f, 0.f, 0.f};
-      prep::tile_acc<true, false>(d, P, LP, dos, kDvLd, m0, n0, C / 8);  // A(i, r) = P[r][i]
+      prep::tile_acc_t<scan::kB16<Tin>, true, false>(d, P, LP, dos, kDvLd, m0, n0, C / 8);  // A(i, r) = P[r][i]
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = m0 + gq + 8 * (e >> 1);
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dh_kernel(
         const int64_t col = v0 + n0 + 2 * tq + (e & 1);
         d[e] = (i < Lc && col < V) ? dvn[((t0 + i) * HV + hv) * V + col] : 0.f;
       }
-      prep::tile_acc<false, false>(d, st.kt, KL, st.hs, LD, m0, n0, (int)(Kp / 8));
+      prep::tile_acc_t<scan::kB16<Tin>, false, false>(d, st.kt, KL, st.hs, LD, m0, n0, (int)(Kp / 8));
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = m0 + gq + 8 * (e >> 1), cc = n0 + 2 * tq + (e & 1);
@@ -239,8 +239,8 @@ __global__ void __launch_bounds__(kThreads) bwd_dh_kernel(
         const int r = m0 + gq + 8 * (e >> 1), cc = n0 + 2 * tq + (e & 1);
         d[e] = st.hs[r * LD + cc] * ((e >> 1) ? e1 : e0);
       }
-      prep::tile_acc<true, false>(d, st.kt, KL, dos, LD, m0, n0, C / 8);
-      prep::tile_acc<true, false>(d, st.ws, WL, st.vn, LD, m0, n0, C / 8);
+      prep::tile_acc_t<scan::kB16<Tin>, true, false>(d, st.kt, KL, dos, LD, m0, n0, C / 8);
+      prep::tile_acc_t<scan::kB16<Tin>, true, false>(d, st.ws, WL, st.vn, LD, m0, n0, C / 8);
       __syncwarp();
       // every warp reads only its own tiles of hs, so the write-back needs no barrier
 #pragma unroll
@@ -592,7 +592,7 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
     for (int tix = warp; tix < MT * (kWt / 8); tix += kWarps) {
       const int mm = 16 * (tix % MT), n0 = 8 * (tix / MT);
       float dd4[4] = {0.f, 0.f, 0.f, 0.f};
-      prep::tile_acc<true, false>(dd4, Tm, LT, dvt, kLdB, mm, n0, C / 8);  // A(i, j) = T[j][i]
+      prep::tile_acc_t<scan::kB16<Tin>, true, false>(dd4, Tm, LT, dvt, kLdB, mm, n0, C / 8);  // A(i, j) = T[j][i]
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = mm + gq + 8 * (e >> 1), c = n0 + 2 * tq + (e & 1);
@@ -611,7 +611,7 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
 #pragma unroll
     for (int s2 = 0; s2 < NAW; ++s2) {
       const int n0 = 8 * ((warp + 8 * s2) / MT);
-      prep::tile_acc<false, true>(fA[s2], dxt, kLdA, ut, kLdA, m0, n0, kWt / 8);  // B(v, j) = u[j][v]
+      prep::tile_acc_t<scan::kB16<Tin>, false, true>(fA[s2], dxt, kLdA, ut, kLdA, m0, n0, kWt / 8);  // B(v, j) = u[j][v]
     }
   }
   // w-path: dY = T^T dW into sY, then acc += dY w^T
@@ -623,7 +623,7 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
     for (int tix = warp; tix < MT * (kWt / 8); tix += kWarps) {
       const int mm = 16 * (tix % MT), n0 = 8 * (tix / MT);
       float dd4[4] = {0.f, 0.f, 0.f, 0.f};
-      prep::tile_acc<true, false>(dd4, Tm, LT, dwt, kLdB, mm, n0, C / 8);
+      prep::tile_acc_t<scan::kB16<Tin>, true, false>(dd4, Tm, LT, dwt, kLdB, mm, n0, C / 8);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = mm + gq + 8 * (e >> 1), c = n0 + 2 * tq + (e & 1);
@@ -637,7 +637,7 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
 #pragma unroll
   for (int s2 = 0; s2 < NAW; ++s2) {
     const int n0 = 8 * ((warp + 8 * s2) / MT);
-    prep::tile_acc<false, true>(fA[s2], sY, KL, wf, KL, m0, n0, (int)(Kp / 8));
+    prep::tile_acc_t<scan::kB16<Tin>, false, true>(fA[s2], sY, KL, wf, KL, m0, n0, (int)(Kp / 8));
   }
   __syncthreads();  // AT (T) is dead: dA goes there
 #pragma unroll

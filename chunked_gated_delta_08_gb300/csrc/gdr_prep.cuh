@@ -113,6 +113,56 @@ __device__ __forceinline__ void tile_acc(float (&d)[4], const float *a, int64_t 
   }
 }
 
+// d += the same product in one bf16 pass (m16n8k16, fp32 accumulation) over
+// 16 nk16 values of k: A(m, k) = TA ? a[k lda + m] : a[m lda + k];
+// B(k, n) = TB ? b[n ldb + k] : b[k ldb + n].  Non-transposed A rows and
+// transposed B rows are read as float pairs (even strides and offsets).
+template <bool TA, bool TB>
+__device__ __forceinline__ void tile_acc_b16(float (&d)[4], const float *a, int64_t lda, const float *b, int64_t ldb,
+                                             int m0, int n0, int nk16) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  for (int ks = 0; ks < nk16; ++ks) {
+    const int k0 = 16 * ks;
+    uint32_t a0, a1, a2, a3, b0, b1;
+    if (TA) {
+      const float *ar = a + (int64_t)(k0 + 2 * t) * lda + m0 + g;
+      a0 = scan::bf16x2(ar[0], ar[lda]);
+      a1 = scan::bf16x2(ar[8], ar[lda + 8]);
+      a2 = scan::bf16x2(ar[8 * lda], ar[9 * lda]);
+      a3 = scan::bf16x2(ar[8 * lda + 8], ar[9 * lda + 8]);
+    } else {
+      const float *ar = a + (int64_t)(m0 + g) * lda + k0 + 2 * t;
+      const float2 x0 = *reinterpret_cast<const float2 *>(ar), x1 = *reinterpret_cast<const float2 *>(ar + 8 * lda),
+                   x2 = *reinterpret_cast<const float2 *>(ar + 8),
+                   x3 = *reinterpret_cast<const float2 *>(ar + 8 * lda + 8);
+      a0 = scan::bf16x2(x0.x, x0.y);
+      a1 = scan::bf16x2(x1.x, x1.y);
+      a2 = scan::bf16x2(x2.x, x2.y);
+      a3 = scan::bf16x2(x3.x, x3.y);
+    }
+    if (TB) {
+      const float *br = b + (int64_t)(n0 + g) * ldb + k0 + 2 * t;
+      const float2 y0 = *reinterpret_cast<const float2 *>(br), y1 = *reinterpret_cast<const float2 *>(br + 8);
+      b0 = scan::bf16x2(y0.x, y0.y);
+      b1 = scan::bf16x2(y1.x, y1.y);
+    } else {
+      const float *br = b + (int64_t)(k0 + 2 * t) * ldb + n0 + g;
+      b0 = scan::bf16x2(br[0], br[ldb]);
+      b1 = scan::bf16x2(br[8 * ldb], br[9 * ldb]);
+    }
+    scan::mma_bf16(d, a0, a1, a2, a3, b0, b1);
+  }
+}
+
+// The accumulating product for the input type: one bf16 pass for bf16 inputs,
+// 3 x TF32 otherwise (nk8 k-steps of 8).
+template <bool B16, bool TA, bool TB>
+__device__ __forceinline__ void tile_acc_t(float (&d)[4], const float *a, int64_t lda, const float *b, int64_t ldb,
+                                           int m0, int n0, int nk8) {
+  if constexpr (B16) tile_acc_b16<TA, TB>(d, a, lda, b, ldb, m0, n0, nk8 / 2);
+  else tile_acc<TA, TB>(d, a, lda, b, ldb, m0, n0, nk8);
+}
+
 // The same with A and B read through functors fa(m, k), fb(k, n) (tile-local
 // indices), for the triangular operands of the solve.
 template <typename FA, typename FB>
