@@ -352,45 +352,90 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
     __syncthreads();
     if (tid < K)
       for (int vv = 0; vv < 32; ++vv) gLacc = fmaf(hB[tid * kQL + vv], dhB[tid * kQL + vv], gLacc);
+    if constexpr (scan::kB16<Tin>) {
+      // one bf16 pass per k-step of 16 (the operands' rows are float pairs: kQL is even)
 #pragma unroll
-    for (int k0 = 0; k0 < 32; k0 += 8) {
-      uint32_t oh[4], ol[4], wh[4], wl[4], nh[4], nl[4];
-      {
-        const float *ar = doA + (m0 + gq) * kQL + k0 + tq;
-        const float *br = dvA + (m0 + gq) * kQL + k0 + tq;
-        const float *cr = vnA + (m0 + gq) * kQL + k0 + tq;
-        const int offs[4] = {0, 8 * kQL, 4, 8 * kQL + 4};
+      for (int k0 = 0; k0 < 32; k0 += 16) {
+        uint32_t oa[4], wa[4], na[4];
+        {
+          const float *ar = doA + (m0 + gq) * kQL + k0 + 2 * tq;
+          const float *br = dvA + (m0 + gq) * kQL + k0 + 2 * tq;
+          const float *cr = vnA + (m0 + gq) * kQL + k0 + 2 * tq;
+          const int offs[4] = {0, 8 * kQL, 8, 8 * kQL + 8};
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          scan::split3(ar[offs[x]], oh[x], ol[x]);
-          scan::split3(br[offs[x]], wh[x], wl[x]);
-          scan::split3(cr[offs[x]], nh[x], nl[x]);
+          for (int x = 0; x < 4; ++x) {
+            const float2 p0 = *reinterpret_cast<const float2 *>(ar + offs[x]);
+            const float2 p1 = *reinterpret_cast<const float2 *>(br + offs[x]);
+            const float2 p2 = *reinterpret_cast<const float2 *>(cr + offs[x]);
+            oa[x] = scan::bf16x2(p0.x, p0.y);
+            wa[x] = scan::bf16x2(p1.x, p1.y);
+            na[x] = scan::bf16x2(p2.x, p2.y);
+          }
+        }
+#pragma unroll
+        for (int s = 0; s < NTW; ++s) {
+          const int tix = warp + 8 * s;
+          const int n0 = 8 * (tix / MT);
+          if (n0 >= 8 * ntk) continue;
+          const float *hb = hB + (n0 + gq) * kQL + k0 + 2 * tq;
+          const float *db = dhB + (n0 + gq) * kQL + k0 + 2 * tq;
+          const float2 h0v = *reinterpret_cast<const float2 *>(hb), h1v = *reinterpret_cast<const float2 *>(hb + 8);
+          const float2 d0v = *reinterpret_cast<const float2 *>(db), d1v = *reinterpret_cast<const float2 *>(db + 8);
+          const uint32_t bh0 = scan::bf16x2(h0v.x, h0v.y), bh1 = scan::bf16x2(h1v.x, h1v.y);
+          const uint32_t bd0 = scan::bf16x2(d0v.x, d0v.y), bd1 = scan::bf16x2(d1v.x, d1v.y);
+          scan::mma_bf16(fQ[s], oa[0], oa[1], oa[2], oa[3], bh0, bh1);
+          scan::mma_bf16(fW[s], wa[0], wa[1], wa[2], wa[3], bh0, bh1);
+          scan::mma_bf16(fK[s], na[0], na[1], na[2], na[3], bd0, bd1);
+        }
+#pragma unroll
+        for (int s = 0; s < NPW; ++s) {
+          const int n0 = 8 * ((warp + 8 * s) / MT);
+          const float *vb = vnA + (n0 + gq) * kQL + k0 + 2 * tq;
+          const float2 v0v = *reinterpret_cast<const float2 *>(vb), v1v = *reinterpret_cast<const float2 *>(vb + 8);
+          scan::mma_bf16(fP[s], oa[0], oa[1], oa[2], oa[3], scan::bf16x2(v0v.x, v0v.y), scan::bf16x2(v1v.x, v1v.y));
         }
       }
+    } else {
 #pragma unroll
-      for (int s = 0; s < NTW; ++s) {
-        const int tix = warp + 8 * s;  // m-tile tix % MT (fixed per warp), n-tile tix / MT
-        const int n0 = 8 * (tix / MT);
-        if (n0 >= 8 * ntk) continue;
-        uint32_t bh[2], bl[2], ch[2], cl[2];
-        const float *hb = hB + (n0 + gq) * kQL + k0 + tq;
-        const float *db = dhB + (n0 + gq) * kQL + k0 + tq;
-        scan::split3(hb[0], bh[0], bl[0]);
-        scan::split3(hb[4], bh[1], bl[1]);
-        scan::split3(db[0], ch[0], cl[0]);
-        scan::split3(db[4], ch[1], cl[1]);
-        scan::mma3(fQ[s], oh, ol, bh, bl);
-        scan::mma3(fW[s], wh, wl, bh, bl);
-        scan::mma3(fK[s], nh, nl, ch, cl);
-      }
+      for (int k0 = 0; k0 < 32; k0 += 8) {
+        uint32_t oh[4], ol[4], wh[4], wl[4], nh[4], nl[4];
+        {
+          const float *ar = doA + (m0 + gq) * kQL + k0 + tq;
+          const float *br = dvA + (m0 + gq) * kQL + k0 + tq;
+          const float *cr = vnA + (m0 + gq) * kQL + k0 + tq;
+          const int offs[4] = {0, 8 * kQL, 4, 8 * kQL + 4};
 #pragma unroll
-      for (int s = 0; s < NPW; ++s) {
-        const int n0 = 8 * ((warp + 8 * s) / MT);
-        uint32_t bh[2], bl[2];
-        const float *vb = vnA + (n0 + gq) * kQL + k0 + tq;
-        scan::split3(vb[0], bh[0], bl[0]);
-        scan::split3(vb[4], bh[1], bl[1]);
-        scan::mma3(fP[s], oh, ol, bh, bl);
+          for (int x = 0; x < 4; ++x) {
+            scan::split3(ar[offs[x]], oh[x], ol[x]);
+            scan::split3(br[offs[x]], wh[x], wl[x]);
+            scan::split3(cr[offs[x]], nh[x], nl[x]);
+          }
+        }
+#pragma unroll
+        for (int s = 0; s < NTW; ++s) {
+          const int tix = warp + 8 * s;  // m-tile tix % MT (fixed per warp), n-tile tix / MT
+          const int n0 = 8 * (tix / MT);
+          if (n0 >= 8 * ntk) continue;
+          uint32_t bh[2], bl[2], ch[2], cl[2];
+          const float *hb = hB + (n0 + gq) * kQL + k0 + tq;
+          const float *db = dhB + (n0 + gq) * kQL + k0 + tq;
+          scan::split3(hb[0], bh[0], bl[0]);
+          scan::split3(hb[4], bh[1], bl[1]);
+          scan::split3(db[0], ch[0], cl[0]);
+          scan::split3(db[4], ch[1], cl[1]);
+          scan::mma3(fQ[s], oh, ol, bh, bl);
+          scan::mma3(fW[s], wh, wl, bh, bl);
+          scan::mma3(fK[s], nh, nl, ch, cl);
+        }
+#pragma unroll
+        for (int s = 0; s < NPW; ++s) {
+          const int n0 = 8 * ((warp + 8 * s) / MT);
+          uint32_t bh[2], bl[2];
+          const float *vb = vnA + (n0 + gq) * kQL + k0 + tq;
+          scan::split3(vb[0], bh[0], bl[0]);
+          scan::split3(vb[4], bh[1], bl[1]);
+          scan::mma3(fP[s], oh, ol, bh, bl);
+        }
       }
     }
   }
