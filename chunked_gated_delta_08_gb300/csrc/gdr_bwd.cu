@@ -177,6 +177,17 @@ __global__ void __launch_bounds__(kThreads) bwd_dh_kernel(
     const int64_t t0 = sr.bos + c * C;
     const int Lc = (int)(sr.eos - t0 < (int64_t)C ? sr.eos - t0 : (int64_t)C);
     const int64_t tl = t0 + Lc - 1;
+    if (c > 0) {  // the previous chunk's rows into L2 while this one runs (it is always whole)
+      const int64_t t1 = t0 - C;
+      const int64_t gwb = (PER_K ? K : 1) * 4;
+      const int vb = (int)((V - v0 < kBVd ? V - v0 : kBVd));
+      scan::prefetch_rows_l2(k + (t1 * H + hq) * K, H * K * (int64_t)sizeof(Tin), C, (int)(K * sizeof(Tin)));
+      scan::prefetch_rows_l2(q + (t1 * H + hq) * K, H * K * (int64_t)sizeof(Tin), C, (int)(K * sizeof(Tin)));
+      scan::prefetch_rows_l2(w + (t1 * HV + hv) * K, HV * K * 4, C, (int)(K * 4));
+      scan::prefetch_rows_l2(gcum + (t1 * HV + hv) * (PER_K ? K : 1), HV * gwb, C, (int)gwb);
+      scan::prefetch_rows_l2(d_o + (t1 * HV + hv) * V + v0, HV * V * (int64_t)sizeof(Tin), C, vb * (int)sizeof(Tin));
+      scan::prefetch_rows_l2(dvn + (t1 * HV + hv) * V + v0, HV * V * 4, C, vb * 4);
+    }
     for (int64_t e = tid; e < K * kBVd; e += kThreads) {
       const int64_t d = e / kBVd, vv = e % kBVd;
       if (v0 + vv < V) dhc[(((cbase + c) * HV + hv) * K + d) * V + v0 + vv] = st.hs[d * LD + vv];

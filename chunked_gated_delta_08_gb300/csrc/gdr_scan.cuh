@@ -93,6 +93,19 @@ __device__ __forceinline__ float exp_(float x) {
 template <typename Tin>
 constexpr bool kB16 = std::is_same<Tin, __nv_bfloat16>::value;
 
+// Asks L2 for `rows` rows of `row_bytes` bytes, `stride` bytes apart, from p
+// (global memory), one 128-byte line per request, spread over the block's
+// 256 threads: a sequential scan issues it for the next chunk so that chunk's
+// row loads find their lines (and address translations) in L2.
+__device__ __forceinline__ void prefetch_rows_l2(const void *p, int64_t stride, int rows, int row_bytes) {
+  const int lines = (row_bytes + 127) >> 7;
+  for (int e = threadIdx.x; e < rows * lines; e += kScanThreads) {
+    const int r = e / lines, l = e - r * lines;
+    const char *a = static_cast<const char *>(p) + (int64_t)r * stride + 128 * l;
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+  }
+}
+
 // Kb rows (L2-normalized k times e^{G_L - G}) into kt and -w into ws, for the
 // chunk's rows, zero past Lc and past K.  Warp w takes rows w, w + 8, ...; the
 // loads of RB rows (KV values per lane and row) are all issued before any row
