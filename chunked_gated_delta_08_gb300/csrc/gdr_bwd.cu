@@ -138,7 +138,8 @@ __global__ void __launch_bounds__(kThreads) bwd_dv_local_kernel(
 }
 
 // --------------------------------------------------------------------------
-// dh: grid (N, HV, ceil(V / 32)), sequential over the sequence's chunks, last
+// dh: one block per (sequence, value head, 32-column V tile), launched longest
+// sequence first (seq_of_rank), sequential over the sequence's chunks, last
 // to first.  Per chunk, on tensor cores (3 x TF32):
 //   dv_new += Kb dh'           (C x 32) = (C x K)(K x 32), Kb = k e^{G_L - G}
 //   dh = e^{G_L} dh' + Qt^T do - w^T dv_new   (K x 32),      Qt = q e^G
@@ -158,7 +159,10 @@ __global__ void __launch_bounds__(kThreads) bwd_dh_kernel(
   float *dos = smem + scan::smem_floats(C, K);
   if (chunk_offsets && chunk_offsets[N] < 0) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, gq = lane >> 2, tq = lane & 3;
-  const int64_t n = blockIdx.x, hv = blockIdx.y, v0 = (int64_t)blockIdx.z * kBVd;
+  // block b: sequence rank b / (HV * nvt), value head, V tile (rank-major, longest sequences first)
+  const int64_t nvt = (V + kBVd - 1) / kBVd, per = HV * nvt;
+  const int64_t n = seq_of_rank(cu, N, (int64_t)blockIdx.x / per);
+  const int64_t hv = ((int64_t)blockIdx.x % per) / nvt, v0 = ((int64_t)blockIdx.x % nvt) * kBVd;
   const int64_t hq = hv / (HV / H);
   const int64_t Kp = scan::kpad(K), WL = scan::ws_ld(K), KL = scan::kt_ld(K);
   const SeqRange sr = seq_range(cu, n, T);
@@ -889,7 +893,7 @@ int launch_bwd_dh(const BwdArgs &a) {
     auto kern = bwd_dh_kernel<Tin, C, PK>;
     int rc = set_smem(kern, smem, "bwd_dh_kernel");
     if (rc != GDR_OK) return rc;
-    kern<<<dim3((unsigned)f.d.N, (unsigned)f.d.HV, (unsigned)cdiv(f.d.V, kBVd)), kThreads, smem, f.stream>>>(
+    kern<<<dim3((unsigned)(f.d.N * f.d.HV * cdiv(f.d.V, kBVd))), kThreads, smem, f.stream>>>(
         (const Tin *)f.q, (const Tin *)f.k, (const Tin *)a.d_o, f.w, f.gcum, a.dht, f.cu, f.chunk_offsets, f.d.N,
         f.d.T, f.d.H, f.d.HV, K, f.d.V, f.l2, a.dvn, a.dhc, a.dh0);
     return after_launch("bwd_dh_kernel");

@@ -264,7 +264,8 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(
 }
 
 // --------------------------------------------------------------------------
-// fwd_h: grid (N, HV, ceil(V / 32)), sequential over the sequence's chunks.
+// fwd_h: one block per (sequence, value head, 32-column V tile), launched
+// longest sequence first (seq_of_rank), sequential over the sequence's chunks.
 // Each chunk's two products run on tensor cores in 3 x TF32 (gdr_scan.cuh).
 // --------------------------------------------------------------------------
 template <typename Tin, int C, bool PER_K>
@@ -277,7 +278,10 @@ __global__ void __launch_bounds__(kThreads) fwd_h_kernel(
   const scan::Tiles st = scan::carve(smem, C, K);
   if (chunk_offsets && chunk_offsets[N] < 0) return;
   const int tid = threadIdx.x;
-  const int64_t n = blockIdx.x, hv = blockIdx.y, v0 = (int64_t)blockIdx.z * kBVh;
+  // block b: sequence rank b / (HV * nvt), value head, V tile (rank-major, longest sequences first)
+  const int64_t nvt = (V + kBVh - 1) / kBVh, per = HV * nvt;
+  const int64_t n = seq_of_rank(cu, N, (int64_t)blockIdx.x / per);
+  const int64_t hv = ((int64_t)blockIdx.x % per) / nvt, v0 = ((int64_t)blockIdx.x % nvt) * kBVh;
   const int64_t hq = hv / (HV / H);
   const int64_t Kp = scan::kpad(K);
   const SeqRange sr = seq_range(cu, n, T);
@@ -478,7 +482,7 @@ static int fwd_h_t(const ChunkedArgs &a) {
     constexpr bool PK = decltype(cfg)::PK;
     const size_t smem = sizeof(float) * scan::smem_floats(CC, K);
     auto kern = fwd_h_kernel<Tin, CC, PK>;
-    dim3 grid((unsigned)a.d.N, (unsigned)a.d.HV, (unsigned)cdiv(V, kBVh));
+    dim3 grid((unsigned)(a.d.N * a.d.HV * cdiv(V, kBVh)));
     int rc = launch_checked(kern, grid, smem, a.stream, "fwd_h_kernel");
     if (rc == GDR_OK && a.d.N > 0) {
       kern<<<grid, kThreads, smem, a.stream>>>((const Tin *)a.k, a.w, a.u, a.gcum, a.h0, a.cu, a.chunk_offsets,

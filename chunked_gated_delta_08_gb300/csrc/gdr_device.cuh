@@ -36,6 +36,32 @@ __device__ __forceinline__ SeqRange seq_range(const int64_t *cu, int64_t n, int6
   return {n * T, (n + 1) * T};
 }
 
+// The sequence a state-scan block takes: blocks are launched in order of rank,
+// and rank r is the r-th longest sequence (ties by index), so the longest
+// scans start in the first wave instead of waiting for slots behind shorter
+// ones.  Ranks are computed in the block for up to kRankedSeqs sequences (one
+// thread per sequence counts the longer ones); beyond that, and in the dense
+// layout (all sequences equal), rank r is sequence r.  Called by every thread
+// of the block (it synchronizes).
+constexpr int kRankedSeqs = 256;
+__device__ __forceinline__ int64_t seq_of_rank(const int64_t *cu, int64_t N, int64_t r) {
+  if (!cu || N > kRankedSeqs || N > (int64_t)blockDim.x) return r;
+  __shared__ long long picked;
+  if (threadIdx.x == 0) picked = r;
+  __syncthreads();
+  if ((int64_t)threadIdx.x < N) {
+    const int64_t n = threadIdx.x, len = cu[n + 1] - cu[n];
+    int64_t rank = 0;
+    for (int64_t m = 0; m < N; ++m) {
+      const int64_t lm = cu[m + 1] - cu[m];
+      rank += (lm > len || (lm == len && m < n)) ? 1 : 0;
+    }
+    if (rank == r) picked = n;
+  }
+  __syncthreads();
+  return picked;
+}
+
 // Maps a chunk row to (sequence, chunk-in-sequence); false if the row is unused.
 __device__ __forceinline__ bool chunk_coords(const int64_t *chunk_indices, int64_t chunk, int64_t T, int C,
                                              int64_t *n, int64_t *j) {
