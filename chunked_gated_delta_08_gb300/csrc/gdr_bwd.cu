@@ -560,7 +560,7 @@ constexpr int kLdA = kWt + 4;    // A operands / B read [n][k] (4 mod 32)
 __host__ __device__ constexpr int64_t wy_scratch_floats(int C, int64_t K, bool per_k) {
   const int64_t KL = scan::kpad(K) + 4;
   const int64_t a = prep::gram_scratch_floats(C, K, per_k);
-  const int64_t b = (int64_t)C * (kLdB + 2 * kLdA);
+  const int64_t b = (int64_t)C * (kLdB + 3 * kLdA);
   const int64_t c = (int64_t)C * (kLdB + KL);
   const int64_t m = a > b ? a : b;
   return (m > c ? m : c) > 1536 ? (m > c ? m : c) : 1536;
@@ -598,7 +598,7 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
   float *up = sY + C * KL;  // then the per-element dGamma
   float *scr = up + C * KL;
   float *Xs = scr, *Ys = scr + 16 * KL;                                     // gram
-  float *dvt = scr, *ut = scr + C * kLdB, *dxt = ut + C * kLdA;             // V tiles
+  float *dvt = scr, *ut = scr + C * kLdB, *dxt = ut + C * kLdA, *vt = dxt + C * kLdA;  // V tiles
   float *dwt = scr, *wf = scr + C * kLdB;                                   // K tiles, w
   float *gtot = up;
   float *dAs = AT;
@@ -647,6 +647,7 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
       const int vok = (int)(V - v0 < kWt ? V - v0 : kWt);
       prep::tile_to_smem(dvt, kLdB, dvn + (t0 * HV + hv) * V + v0, HV * V, C, kWt, Lc, vok);
       prep::tile_to_smem(ut, kLdA, u + (t0 * HV + hv) * V + v0, HV * V, C, kWt, Lc, vok);
+      prep::tile_to_smem(vt, kLdA, v + (t0 * HV + hv) * V + v0, HV * V, C, kWt, Lc, vok);
     }
     __syncthreads();
     for (int tix = warp; tix < MT * (kWt / 8); tix += kWarps) {
@@ -661,11 +662,8 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
       }
     }
     __syncthreads();
-    for (int i = warp; i < Lc; i += kWarps) {
-      float sacc = 0.f;
-      const int64_t col = v0 + lane;
-      if (col < V) sacc = dxt[i * kLdA + lane] * to_f32(v[((t0 + i) * HV + hv) * V + col]);
-      sacc = warp_sum(sacc);
+    for (int i = warp; i < Lc; i += kWarps) {  // v rows from the tile (zero past V)
+      const float sacc = warp_sum(dxt[i * kLdA + lane] * vt[i * kLdA + lane]);
       if (lane == 0) dbs[i] += sacc;
     }
 #pragma unroll
