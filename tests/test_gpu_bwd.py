@@ -106,6 +106,19 @@ def test_bwd_cases(gdr, case, dtype):
     assert_parity(got, ref, dtype, str(case))
 
 
+def test_bwd_many_varied_sequences(gdr):
+    """The reverse scan's longest-first block order over 40 mixed-length
+    sequences (per-key gate, bf16) against the oracle's reverse recurrence."""
+    rng = np.random.default_rng(7)
+    lengths = [int(x) for x in rng.integers(1, 150, size=40)]
+    lengths[5] = 500
+    _, x = wl.random_case(1, sum(lengths), 2, 2, 32, 48, dtype=torch.bfloat16, lengths=lengths, gate_per_k=True,
+                          seed=17, grads=True)
+    got = run_gpu(gdr, x, x["do"], x["dht"], 64, True)
+    ref = run_ref(x, x["do"], x["dht"], True)
+    assert_parity(got, ref, torch.bfloat16, "40 sequences")
+
+
 def test_bwd_without_dht_and_h0(gdr):
     w, x = wl.random_case(1, 130, 1, 2, 64, 64, dtype=torch.float32, use_h0=False, seed=5, grads=True)
     got = run_gpu(gdr, x, x["do"], None, 64, True)

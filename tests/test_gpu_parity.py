@@ -98,6 +98,22 @@ def test_varlen_equals_separate_runs_bitwise(gdr):
             assert torch.equal(hp[0], ht[n]), f"{algo}: ht of sequence {n} differs from its separate run"
 
 
+@pytest.mark.parametrize("N", [37, 300], ids=["ranked", "beyond_rank_limit"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+def test_many_varied_sequences(gdr, N, dtype):
+    """Many sequences of mixed lengths (the state scans launch their blocks
+    longest sequence first, ranking up to 256 sequences in the block and
+    taking index order beyond that): both paths against the oracle."""
+    rng = np.random.default_rng(61 + N)
+    lengths = [int(x) for x in rng.integers(1, 200, size=N)]
+    lengths[N // 2] = 700  # one long sequence among short ones
+    T = sum(lengths)
+    _, x = wl.random_case(1, T, 2, 2, 32, 48, dtype=dtype, lengths=lengths, gate_per_k=(N == 37), seed=N)
+    o, ht = run_gpu(gdr, x, 64, True, "chunked")
+    ref = run_ref(x, True)
+    assert_parity(o, ht, ref, dtype, f"{N} sequences")
+
+
 # ---------------------------------------------------------------- large dense workload, every unit
 @pytest.mark.parametrize("algo", ["chunked", "fused"])
 def test_large_dense_all_units(gdr, algo):
