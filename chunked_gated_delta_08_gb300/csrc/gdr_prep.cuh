@@ -11,6 +11,8 @@
 // Pages cited: the coverage guide = "FLA 算子内核正确性测试与覆盖矩阵" (fla/ops correctness-coverage guide).
 #pragma once
 
+#include <type_traits>
+
 #include "gdr_scan.cuh"
 
 namespace gdr {
@@ -340,13 +342,70 @@ struct TileRegs {
   }
 };
 
+// Four consecutive elements of a bf16 or fp32 row as floats (16- or 8-byte load).
+template <typename Tin>
+__device__ __forceinline__ float4 load4(const Tin *p) {
+  if constexpr (std::is_same<Tin, float>::value) {
+    return *reinterpret_cast<const float4 *>(p);
+  } else {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+}
+
+// The rows of load_qk_rows with vector loads, for K % 4 == 0, K <= 128, row
+// stride xl % 4 == 0 and q, k aligned to 16 bytes: lane l takes keys 4l ..
+// 4l + 3, and all of a warp's rows (C / 8) have their loads in flight at once.
+template <typename Tin, int C>
+__device__ __forceinline__ void load_qk_rows_vec(const Tin *__restrict__ q, const Tin *__restrict__ k, int64_t t0,
+                                                 int Lc, int64_t H, int64_t hq, int64_t K, int l2, float *qs,
+                                                 float *ks, int64_t xl) {
+  constexpr int kWarps = 8, RPW = C / kWarps;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t width = scan::kpad(K) + 4;
+  const int d0 = 4 * lane;
+  float4 qv[RPW], kv[RPW];
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) {
+    const int i = warp + kWarps * r;
+    const bool ok = i < Lc && d0 < K;
+    const int64_t off = ((t0 + i) * H + hq) * K + d0;
+    qv[r] = (q && ok) ? load4(q + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+    kv[r] = ok ? load4(k + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) {
+    const int i = warp + kWarps * r;
+    const float sq = qv[r].x * qv[r].x + qv[r].y * qv[r].y + qv[r].z * qv[r].z + qv[r].w * qv[r].w;
+    const float sk = kv[r].x * kv[r].x + kv[r].y * kv[r].y + kv[r].z * kv[r].z + kv[r].w * kv[r].w;
+    const float cq = l2 ? rsqrtf(warp_sum(sq) + kL2Eps) : 1.f, ck = l2 ? rsqrtf(warp_sum(sk) + kL2Eps) : 1.f;
+    if (d0 < width) {  // zero past K up to the padded width
+      if (q) *reinterpret_cast<float4 *>(qs + i * xl + d0) = make_float4(qv[r].x * cq, qv[r].y * cq, qv[r].z * cq, qv[r].w * cq);
+      *reinterpret_cast<float4 *>(ks + i * xl + d0) = make_float4(kv[r].x * ck, kv[r].y * ck, kv[r].z * ck, kv[r].w * ck);
+    }
+    if (lane == 0 && width > 128) {  // the last padding columns past lane 31's keys
+      if (q) *reinterpret_cast<float4 *>(qs + i * xl + 128) = make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4 *>(ks + i * xl + 128) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+}
+
 // Rows of q (optional) and k, L2-normalized if asked, zero past Lc and past K,
 // into qs and ks (row stride xl >= kpad(K) + 4).  Four rows per warp have
-// their loads in flight before any row is reduced.  All 256 threads.
+// their loads in flight before any row is reduced (all of them, with vector
+// loads, where load_qk_rows_vec applies).  All 256 threads.
 template <typename Tin, int C>
 __device__ __forceinline__ void load_qk_rows(const Tin *__restrict__ q, const Tin *__restrict__ k, int64_t t0,
                                              int Lc, int64_t H, int64_t hq, int64_t K, int l2, float *qs,
                                              float *ks, int64_t xl) {
+  if (K <= 128 && K % 4 == 0 && xl % 4 == 0 &&
+      ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(qs) |
+        reinterpret_cast<uintptr_t>(ks)) & 15u) == 0) {
+    load_qk_rows_vec<Tin, C>(q, k, t0, Lc, H, hq, K, l2, qs, ks, xl);
+    return;
+  }
   constexpr int kWarps = 8;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t width = scan::kpad(K) + 4;
