@@ -167,33 +167,8 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(
   const int nk = (int)(Kp / 8);
   (void)nk;
 
-  // ---- k rows (normalized), g, beta: four rows per warp in flight at a time
-  for (int i0 = warp; i0 < C; i0 += 4 * kWarps) {
-    float kv[4][8];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int i = i0 + kWarps * r;
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int64_t d = lane + 32 * m;
-        kv[r][m] = (i < C && i < Lc && d < K) ? to_f32(k[((t0 + i) * H + hq) * K + d]) : 0.f;
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int i = i0 + kWarps * r;
-      if (i >= C) break;
-      float ss = 0.f;
-#pragma unroll
-      for (int m = 0; m < 8; ++m) ss = fmaf(kv[r][m], kv[r][m], ss);
-      const float sc = l2 ? rsqrtf(warp_sum(ss) + kL2Eps) : 1.f;
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int64_t d = lane + 32 * m;
-        if (d < KL) ks[i * KL + d] = kv[r][m] * sc;  // zero past K and past Lc
-      }
-    }
-  }
+  // ---- k rows (normalized), g, beta
+  prep::load_qk_rows<Tin, C>(nullptr, k, t0, Lc, H, hq, K, l2, nullptr, ks, KL);
   prep::tile_to_smem(gam, GL, g + (t0 * HV + hv) * gw, HV * gw, C, (int)gw, Lc, (int)gw);
   for (int i = tid; i < C; i += kThreads) bet[i] = i < Lc ? load_beta(beta, (t0 + i) * HV + hv, beta_logits) : 0.f;
   __syncthreads();
