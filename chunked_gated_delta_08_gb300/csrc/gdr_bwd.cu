@@ -117,7 +117,8 @@ __global__ void __launch_bounds__(kThreads) bwd_dv_local_kernel(
   for (int e = tid; e < C * LP; e += kThreads) P[e] = 0.f;  // P^T reads the upper part
   __syncthreads();
   // P_ri = sum_d q_rd k_id exp(G_rd - G_id), i <= r < Lc
-  prep::decayed_gram<C, PER_K, false, scan::kB16<Tin>>(qs, ks, KL, gam, GL, K, Lc, nullptr, P, LP, Xs, Ys);
+  prep::decayed_gram<C, PER_K, false, scan::kB16<Tin>, scan::kB16<Tin>>(qs, ks, KL, gam, GL, K, Lc, nullptr, P, LP,
+                                                                          Xs, Ys);
   for (int64_t v0 = 0; v0 < V; v0 += 32) {
     __syncthreads();
     prep::tile_to_smem(dos, kDvLd, d_o + (t0 * HV + hv) * V + v0, HV * V, C, 32, Lc,

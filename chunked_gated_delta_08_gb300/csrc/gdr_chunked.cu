@@ -337,7 +337,8 @@ __global__ void __launch_bounds__(kThreads) fwd_o_kernel(
   prep::tile_to_smem(gam, GL, gcum + (t0 * HV + hv) * gw, HV * gw, C, (int)gw, Lc, (int)gw);
   for (int e = tid; e < C * LP; e += kThreads) P[e] = 0.f;  // the product reads P's upper part too
   __syncthreads();
-  prep::decayed_gram<C, PER_K, false, scan::kB16<Tin>>(qs, ks, KL, gam, GL, K, Lc, nullptr, P, LP, Xs, Ys);
+  prep::decayed_gram<C, PER_K, false, scan::kB16<Tin>, scan::kB16<Tin>>(qs, ks, KL, gam, GL, K, Lc, nullptr, P, LP,
+                                                                          Xs, Ys);
   // q * e^G in place
   for (prep::Walk2D wk(tid, kThreads, (int)Kp); wk.r < C; wk.next()) {
     const int i = wk.r, d = wk.c;

@@ -464,8 +464,10 @@ __host__ __device__ constexpr int64_t gram_scratch_floats(int C, int64_t K, bool
 // blocks entry by entry; block row a > 0 against rows 0 .. 16a-1 as one
 // product of X_i e^{G_i - G_r} and Y_j e^{G_r - G_j}, r = 16 a, so no factor
 // has a positive exponent for non-positive gates.  FAST takes the hardware
-// exponential (the bf16 path).  All 256 threads; ends with a barrier.
-template <int C, bool PER_K, bool STRICT, bool FAST = false>
+// exponential and B16 one bf16 pass for the tile products (the bf16 path; B16
+// only where the result is itself rounded to bf16 next, as P is).  All 256
+// threads; ends with a barrier.
+template <int C, bool PER_K, bool STRICT, bool FAST = false, bool B16 = false>
 __device__ void decayed_gram(const float *X, const float *Y, int64_t xl, const float *gam, int64_t gl, int64_t K,
                              int Lc, const float *s, float *out, int lo, float *Xs, float *Ys) {
   constexpr int kWarps = 8;
@@ -483,7 +485,8 @@ __device__ void decayed_gram(const float *X, const float *Y, int64_t xl, const f
       }
       const int m0 = 16 * a, n0 = 8 * rem;
       float d[4];
-      tile<true>(d, X, xl, Y, xl, m0, n0, nk);
+      if constexpr (B16) tile_b16<true>(d, X, xl, Y, xl, m0, n0, nk / 2);
+      else tile<true>(d, X, xl, Y, xl, m0, n0, nk);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = m0 + gq + 8 * (e >> 1), j = n0 + 2 * tq + (e & 1);
@@ -541,7 +544,8 @@ __device__ void decayed_gram(const float *X, const float *Y, int64_t xl, const f
     __syncthreads();
     for (int nt = warp; nt < r / 8; nt += kWarps) {
       float d[4];
-      tile<true>(d, Xs, xl, Ys, xl, 0, 8 * nt, nk);
+      if constexpr (B16) tile_b16<true>(d, Xs, xl, Ys, xl, 0, 8 * nt, nk / 2);
+      else tile<true>(d, Xs, xl, Ys, xl, 0, 8 * nt, nk);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = r + gq + 8 * (e >> 1), j = 8 * nt + 2 * tq + (e & 1);
