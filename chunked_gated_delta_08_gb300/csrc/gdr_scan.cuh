@@ -161,6 +161,8 @@ __device__ __forceinline__ void load_rows(const Tiles &s, const Tin *__restrict_
 // The same rows with vector loads, for K % 4 == 0, K <= 128 and 16-byte
 // aligned k, w and gcum: lane l takes the four keys 4l .. 4l + 3 of a row (one
 // load per row and tensor instead of four), four rows per warp in flight.
+// It also loads G_L itself (it does not read s.gl) and writes s.gl, visible to
+// the block after the caller's next barrier.
 template <typename Tin, int C, bool PER_K>
 __device__ __forceinline__ void load_rows_vec(const Tiles &s, const Tin *__restrict__ k, const float *__restrict__ w,
                                               const float *__restrict__ gcum, int64_t t0, int Lc, int64_t hv,
@@ -171,6 +173,18 @@ __device__ __forceinline__ void load_rows_vec(const Tiles &s, const Tin *__restr
   const int64_t Kp = kpad(K), WL = ws_ld(K), KL = kt_ld(K);
   const int d0 = 4 * lane;
   const bool lane_in = d0 < K;
+  // G at the chunk's last valid row, for this lane's keys (warp 0 also publishes it in s.gl)
+  float4 gl = make_float4(0.f, 0.f, 0.f, 0.f);
+  {
+    const int64_t tl = t0 + Lc - 1;
+    if (PER_K) {
+      if (lane_in) gl = *reinterpret_cast<const float4 *>(gcum + (tl * HV + hv) * K + d0);
+    } else {
+      const float x = gcum[tl * HV + hv];
+      gl = make_float4(x, x, x, x);
+    }
+    if (warp == 0 && d0 < Kp) *reinterpret_cast<float4 *>(s.gl + d0) = lane_in ? gl : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
 #pragma unroll
   for (int jb = 0; jb < RPW; jb += RB) {
     float kv[RB][4], gv[RB][4], wv[RB][4];
@@ -225,7 +239,6 @@ __device__ __forceinline__ void load_rows_vec(const Tiles &s, const Tin *__restr
         const bool ok = lane_in && i < Lc;
         float4 kb = make_float4(0.f, 0.f, 0.f, 0.f), nw = kb;
         if (ok) {
-          const float4 gl = *reinterpret_cast<const float4 *>(s.gl + d0);
           kb = make_float4(kv[r][0] * sc * exp_<kB16<Tin>>(gl.x - gv[r][0]), kv[r][1] * sc * exp_<kB16<Tin>>(gl.y - gv[r][1]),
                            kv[r][2] * sc * exp_<kB16<Tin>>(gl.z - gv[r][2]), kv[r][3] * sc * exp_<kB16<Tin>>(gl.w - gv[r][3]));
           nw = make_float4(-wv[r][0], -wv[r][1], -wv[r][2], -wv[r][3]);
@@ -240,14 +253,16 @@ __device__ __forceinline__ void load_rows_vec(const Tiles &s, const Tin *__restr
 // The row loader for the shape: vector loads where K % 4 == 0, K <= 128 and
 // k, w, gcum are 16-byte aligned (every row then starts on a 16-byte, bf16 k
 // an 8-byte, boundary), else the scalar loaders.
+template <typename Tin>
+__device__ __forceinline__ bool rows_vec_ok(const Tin *k, const float *w, const float *gcum, int64_t K) {
+  return K <= 128 && K % 4 == 0 &&
+         ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(gcum)) & 15u) == 0;
+}
 template <typename Tin, int C, bool PER_K>
 __device__ __forceinline__ void load_rows_auto(const Tiles &s, const Tin *__restrict__ k, const float *__restrict__ w,
                                                const float *__restrict__ gcum, int64_t t0, int Lc, int64_t hv,
                                                int64_t hq, int64_t H, int64_t HV, int64_t K, int l2) {
-  const bool vec = K <= 128 && K % 4 == 0 &&
-                   ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(gcum)) &
-                    15u) == 0;
-  if (vec) load_rows_vec<Tin, C, PER_K>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
+  if (rows_vec_ok(k, w, gcum, K)) load_rows_vec<Tin, C, PER_K>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
   else if (K <= 128) load_rows<Tin, C, PER_K, 4, 4>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
   else load_rows<Tin, C, PER_K, 8, 2>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
 }
@@ -267,26 +282,35 @@ __device__ __forceinline__ void chunk_step(const Tiles &s, const Tin *__restrict
   const int64_t Kp = kpad(K), WL = ws_ld(K), KL = kt_ld(K);
   const int64_t gw = PER_K ? K : 1;
   const int64_t tl = t0 + Lc - 1;
-  for (int64_t d = tid; d < Kp; d += kScanThreads)
-    s.gl[d] = d < K ? gcum[(tl * HV + hv) * gw + (PER_K ? d : 0)] : 0.f;
-  __syncthreads();
-  // Kb and -w, zero past Lc and past K
   constexpr int kWarps = kScanThreads / 32;
-  load_rows_auto<Tin, C, PER_K>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
-  __syncthreads();
-
-  // ---- v_new = u - w h: C x 32, warp -> rows 16 (warp & 3) .., columns 16 (warp >> 2) ..
+  // u (the start of v_new) for this warp's tile, loaded first so its round trip overlaps the rows'
+  const int m0v = 16 * (warp % (C / 16)), n0v = 16 * (warp / (C / 16));
+  float acc[2][4];
   if (warp < 2 * (C / 16)) {
-    const int m0 = 16 * (warp % (C / 16)), n0 = 16 * (warp / (C / 16));
-    float acc[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int i = m0 + g + 8 * (e >> 1);
-        const int64_t col = c0col + n0 + 8 * nt + 2 * tq + (e & 1);
+        const int i = m0v + g + 8 * (e >> 1);
+        const int64_t col = c0col + n0v + 8 * nt + 2 * tq + (e & 1);
         acc[nt][e] = (i < Lc && col < ucols) ? u[((t0 + i) * HV + hv) * V + col] : 0.f;
       }
+  }
+  // Kb and -w, zero past Lc and past K; G_L per key into s.gl
+  if (rows_vec_ok(k, w, gcum, K)) {
+    load_rows_vec<Tin, C, PER_K>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
+  } else {
+    for (int64_t d = tid; d < Kp; d += kScanThreads)
+      s.gl[d] = d < K ? gcum[(tl * HV + hv) * gw + (PER_K ? d : 0)] : 0.f;
+    __syncthreads();
+    if (K <= 128) load_rows<Tin, C, PER_K, 4, 4>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
+    else load_rows<Tin, C, PER_K, 8, 2>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
+  }
+  __syncthreads();
+
+  // ---- v_new = u - w h: C x 32, warp -> rows 16 (warp & 3) .., columns 16 (warp >> 2) ..
+  if (warp < 2 * (C / 16)) {
+    const int m0 = m0v, n0 = n0v;
     if constexpr (kB16<Tin>) {
       for (int64_t k0 = 0; k0 < Kp; k0 += 16) {
         const float *a = s.ws + (m0 + g) * WL + k0 + 2 * tq;
