@@ -30,9 +30,9 @@
 //               the output epilogue of chunk c (staged in the v_new tile,
 //               written by two TMA tensor stores);
 //   warps 4-11  prep: everything of chunk c that does not need the state
-//               (A, the solve, W', U', P), so it can start chunk c+1 while
-//               the tensor cores turn W', U' into w, u; the chain warps give
-//               it each chunk's norms, gate cumsum and scalars one chunk ahead;
+//               (the q and k norms, gate cumsum and scale vectors, A, the
+//               solve, W', U', P), so it can start chunk c+1 while the
+//               tensor cores turn W', U' into w, u;
 //   warp 12     producer: TMA loads of q, k (3-slot ring) and v (1 slot), g, beta;
 //   warp 13     MMA issuer: one thread issues every tcgen05.mma in a fixed order.
 // Hand-offs are mbarriers, each completing once per chunk.  Every wait is
@@ -96,8 +96,9 @@ constexpr uint32_t TM_S = 0, TM_W = 64, TM_VN = 128, TM_O1 = 192, TM_O2 = 256, T
 
 struct Small {
   float gb[kQKSlots][2][C];     // g, beta of each QK slot (producer)
-  // per-chunk scalars, written by the chain warps one chunk ahead (bw, cw by
-  // chunk parity: the prep warps still read chunk c's while chunk c+1's land)
+  // per-chunk scalars, written by the prep warps at the start of their chunk
+  // (bw, cw by chunk parity; sv, so, gL by chunk mod 3, which the chain warps
+  // read for chunks behind the prep warps')
   float gam[C], rq[C], rk[C];   // gate cumsum and norm scales (0 past the chunk end)
   float bw[2][C];               // beta (0 past the chunk end)
   float ep[C], em[C];           // decay factors e^{G - m}, e^{m - G}
@@ -107,7 +108,7 @@ struct Small {
   float gL[4];                  // chain: G at the chunk's last valid row
   float X[32 * kXL];            // solve scratch
   uint64_t full_qk[kQKSlots], empty_qk[kQKSlots], full_v, empty_v;
-  uint64_t b_s, b_sfree, b_prep, b_w, b_wepi, b_pend, b_vn, b_vnepi, b_h, b_state, b_oepi, b_scal, b_final;
+  uint64_t b_s, b_sfree, b_prep, b_w, b_wepi, b_pend, b_vn, b_vnepi, b_h, b_state, b_oepi, b_final;
   uint32_t tmem_slot;
   int err;
   int bad;
@@ -321,74 +322,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok = t == 0 ? mbar_wait(smem_u32(bar), parity, err, tmo) : true;
       return named_bar_and(kBarChain, 128, ok);
     };
-    // Norms, gate cumsum and per-chunk scalars of chunk cc, once its [K;Q]K^T is in TMEM: q row
-    // norms (2 threads per row), k row norms from diag(K K^T) (TMEM lanes 0-63 = warps 0-1),
-    // the gate cumsum (warp 0); then the scale vectors.  Arrives on b_scal.
-    auto scalars = [&](int cc) -> bool {
-      const int slot = cc % kQKSlots, k3 = cc % 3, par = cc & 1;
-      const int64_t t0 = bos + (int64_t)cc * C;
-      const int L = (int)(eos - t0 < C ? eos - t0 : C);
-      const uint8_t *qk = sm + OFF_QK + slot * SZ_QK;
-      if (!vote_wait(&S.b_s, cc & 1)) return false;
-      tc_fence_after();
-      {
-        const int row = t >> 1, half = t & 1;
-        const uint8_t *qb = qk + 8192 + half * 16384;
-        float ss = 0.f;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) ss += sumsq_bf16x8(ld_sw128_chunk(qb, row, ch));
-        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        if (half == 0) S.rq[row] = row < L ? (p.l2 ? rsqrtf(ss + kL2Eps) : 1.f) : 0.f;
-      }
-      if (warp == 0) {
-        float x0 = S.gb[slot][0][lane], x1 = S.gb[slot][0][lane + 32];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y0 = __shfl_up_sync(0xffffffffu, x0, o), y1 = __shfl_up_sync(0xffffffffu, x1, o);
-          if (lane >= o) {
-            x0 += y0;
-            x1 += y1;
-          }
-        }
-        x1 += __shfl_sync(0xffffffffu, x0, 31);
-        S.gam[lane] = x0;
-        S.gam[lane + 32] = x1;
-      }
-      if (warp < 2) {  // lanes 0-63 of S hold K K^T; its diagonal is |k_i|^2
-        const int i = t;
-        float r32[32];
-        tmem_ld32(lane_addr + TM_S + 32 * (i >> 5), r32);
-        tmem_ld_wait();
-        float kk = 0.f;
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (e == (i & 31)) kk = r32[e];
-        S.rk[i] = i < L ? (p.l2 ? rsqrtf(kk + kL2Eps) : 1.f) : 0.f;
-      }
-      tc_fence_before();
-      named_bar(kBarChain, 128);
-      {
-        const float g0 = S.gam[0], gl = S.gam[L - 1];
-        const float m = 0.5f * (g0 + gl);
-        if (t < 64) {
-          const float gi = S.gam[t];
-          S.sv[k3][t] = t < L ? S.rk[t] * __expf(gl - gi) : 0.f;
-          S.so[k3][t] = S.rq[t] * __expf(gi);
-          S.ep[t] = __expf(gi - m);
-          S.em[t] = __expf(m - gi);
-          const float bw = t < L ? S.gb[slot][1][t] : 0.f;
-          S.bw[par][t] = bw;
-          S.cw[par][t] = bw * __expf(gi) * S.rk[t];
-          if (t == 0) {
-            S.gL[k3] = gl;
-            S.factored = (g0 - gl) <= 160.f;
-          }
-        }
-      }
-      named_bar(kBarChain, 128);
-      if (t == 0) mbar_arrive(smem_u32(&S.b_scal));
-      return true;
-    };
     // h_0 into TMEM (fp32) and its bf16 copy into sH
     {
       const float *src = p.h0 ? p.h0 + (unit * DK + t) * DV : nullptr;
@@ -410,12 +343,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(smem_u32(&S.b_state));
       mbar_arrive(smem_u32(&S.b_vnepi));
     }
-    bool ok = nch == 0 || scalars(0);
+    bool ok = true;
     for (int c = 0; ok && c < nch; ++c) {
       const uint32_t ph = c & 1;
       const int k3 = c % 3;
       // the next chunk's scalars while the prep warps work on this one
-      if (c + 1 < nch && !(ok = scalars(c + 1))) break;
       // the previous output tile in sVN must have been read by its TMA store
       if (t == 0) bulk_wait_read0();
       // w^T of chunk c is in TMEM (its MMAs follow the prep warps' b_prep arrival)
@@ -577,9 +509,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
       }
-      // ---- this chunk's norms, gate cumsum and scalars, from the chain warps
-      if (!vote_wait(&S.b_scal, ph)) break;
-      const int par = c & 1;
+      // ---- this chunk's norms, gate cumsum and scale vectors: q row norms (two threads per
+      //      row), k row norms from the diagonal of K K^T in TMEM lanes 0-63 (prep warps 4-5),
+      //      the gate cumsum (prep warp 0); then one row of each vector per thread of the first
+      //      two prep warps
+      const int par = c & 1, k3 = c % 3;
+      {
+        if (pt < 128) {
+          const int row = pt >> 1, half = pt & 1;
+          const uint8_t *qb = qk + 8192 + half * 16384;
+          float ss = 0.f;
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) ss += sumsq_bf16x8(ld_sw128_chunk(qb, row, ch));
+          ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+          if (half == 0) S.rq[row] = row < L ? (p.l2 ? rsqrtf(ss + kL2Eps) : 1.f) : 0.f;
+        }
+        if (pt >= 128 && pt < 160) {  // one warp: the inclusive cumsum of g over the chunk
+          const int ln = pt - 128;
+          float x0 = S.gb[slot][0][ln], x1 = S.gb[slot][0][ln + 32];
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const float y0 = __shfl_up_sync(0xffffffffu, x0, o), y1 = __shfl_up_sync(0xffffffffu, x1, o);
+            if (ln >= o) {
+              x0 += y0;
+              x1 += y1;
+            }
+          }
+          x1 += __shfl_sync(0xffffffffu, x0, 31);
+          S.gam[ln] = x0;
+          S.gam[ln + 32] = x1;
+        }
+        if (colh == 0 && quad < 2) {  // TMEM lanes 0-63 of S hold K K^T; its diagonal is |k_i|^2
+          const int i = lrow;
+          float r32[32];
+          tmem_ld32(lane_addr + TM_S + 32 * quad, r32);
+          tmem_ld_wait();
+          float kk = 0.f;
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (e == (i & 31)) kk = r32[e];
+          S.rk[i] = i < L ? (p.l2 ? rsqrtf(kk + kL2Eps) : 1.f) : 0.f;
+        }
+        named_bar(kBarPrep, kPrepThreads);
+        if (pt < 64) {
+          const float g0 = S.gam[0], gl = S.gam[L - 1];
+          const float m = 0.5f * (g0 + gl);
+          const float gi = S.gam[pt];
+          S.sv[k3][pt] = pt < L ? S.rk[pt] * __expf(gl - gi) : 0.f;
+          S.so[k3][pt] = S.rq[pt] * __expf(gi);
+          S.ep[pt] = __expf(gi - m);
+          S.em[pt] = __expf(m - gi);
+          const float bw = pt < L ? S.gb[slot][1][pt] : 0.f;
+          S.bw[par][pt] = bw;
+          S.cw[par][pt] = bw * __expf(gi) * S.rk[pt];
+          if (pt == 0) {
+            S.gL[k3] = gl;
+            S.factored = (g0 - gl) <= 160.f;
+          }
+        }
+        named_bar(kBarPrep, kPrepThreads);
+      }
       const bool factored = S.factored;
       // ---- A from lanes 0-63 of S: A_ij = beta_i rk_i rk_j e^{G_i - G_j} (k_i . k_j), i > j;
       //      P from lanes 64-127: P_rj = rq_r rk_j e^{G_r - G_j} (q_r . k_j), j <= r, kept packed in
