@@ -88,8 +88,9 @@ __host__ __device__ constexpr int64_t dv_local_smem_floats(int C, int64_t K, boo
          prep::gram_scratch_floats(C, K, per_k);
 }
 
+// The per-key gate's shared memory allows one block an SM, the scalar gate's two.
 template <typename Tin, int C, bool PER_K>
-__global__ void __launch_bounds__(kThreads) bwd_dv_local_kernel(
+__global__ void __launch_bounds__(kThreads, PER_K ? 1 : 2) bwd_dv_local_kernel(
     const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ d_o,
     const float *__restrict__ gcum, const int64_t *__restrict__ cu, const int64_t *__restrict__ chunk_indices,
     int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V, int l2, float *__restrict__ dvn) {
@@ -148,8 +149,10 @@ __global__ void __launch_bounds__(kThreads) bwd_dv_local_kernel(
 // smem: the scan tiles (dh in hs, Kb then Qt in kt, -w in ws, dv_new in vn,
 //       G_L in gl) | dos[C][40]
 // --------------------------------------------------------------------------
+// At most 128 registers a thread, so that two blocks share an SM and every block
+// of the longest sequence is resident from the start.
 template <typename Tin, int C, bool PER_K>
-__global__ void __launch_bounds__(kThreads) bwd_dh_kernel(
+__global__ void __launch_bounds__(kThreads, 2) bwd_dh_kernel(
     const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ d_o,
     const float *__restrict__ w, const float *__restrict__ gcum, const float *__restrict__ dht,
     const int64_t *__restrict__ cu, const int64_t *__restrict__ chunk_offsets, int64_t N, int64_t T, int64_t H,
@@ -573,8 +576,9 @@ __host__ __device__ constexpr int64_t wy_smem_floats(int C, int64_t K, bool per_
          wy_scratch_floats(C, K, per_k);
 }
 
+// Its shared memory allows one block an SM: one block's worth of registers (no cap at 128).
 template <typename Tin, int C, bool PER_K>
-__global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
+__global__ void __launch_bounds__(kThreads, 1) bwd_wy_kernel(
     const Tin *__restrict__ k, const Tin *__restrict__ v, const Tin *__restrict__ beta,
     const float *__restrict__ dvn, const float *__restrict__ dW, const float *__restrict__ u,
     const float *__restrict__ w, const float *__restrict__ gcum, const int64_t *__restrict__ cu,
@@ -613,6 +617,9 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
   const int64_t gw = PER_K ? K : 1;
   const int d = tid & (kKmax - 1), i_base = tid / kKmax;
   const int m0 = 16 * (warp % MT);
+  // this chunk's rows of the accumulated dk (and dGamma) are read at the end: into L2 now
+  scan::prefetch_rows_l2(dka + (t0 * HV + hv) * K, HV * K * 4, Lc, (int)(K * 4));
+  if (PER_K) scan::prefetch_rows_l2(dga + (t0 * HV + hv) * K, HV * K * 4, Lc, (int)(K * 4));
 
   prep::load_qk_rows<Tin, C>(nullptr, k, t0, Lc, H, hq, K, l2, nullptr, ks, KL);
   prep::tile_to_smem(gam, GL, gcum + (t0 * HV + hv) * gw, HV * gw, C, (int)gw, Lc, (int)gw);
@@ -736,20 +743,32 @@ __global__ void __launch_bounds__(kThreads) bwd_wy_kernel(
   prep::decayed_apply<C, PER_K, true, scan::kB16<Tin>>(dAs, LA, ks, ks, KL, gam, GL, K, Lc, lo, up, KL, scr,
                                                        scr + 16 * KL);
   if (d < K) {
+    // the accumulated dk (and per-key dGamma) of this thread's entries, read in two batches so
+    // that the loads of a batch are in flight together
 #pragma unroll
-    for (int m = 0; m < MQ; ++m) {
-      const int i = 2 * m + i_base;
-      if (i >= Lc) continue;
-      const float gi = PER_K ? gam[i * GL + d] : gam[i];
-      const float eG = scan::exp_<scan::kB16<Tin>>(gi), kv = ks[i * KL + d], y = yv[m];
-      float dk = bet[i] * y * eG;
-      float dgm = dk * kv;
-      const float t1 = lo[i * KL + d], t2 = up[i * KL + d];
-      dk += t1 + t2;
-      dgm += kv * (t1 - t2);
-      const int64_t row = (t0 + i) * HV + hv;
-      dka[row * K + d] += dk;
-      gtot[i * KL + d] = PER_K ? dga[row * K + d] + dgm : dgm;  // this thread's own entry of up
+    for (int hb = 0; hb < 2; ++hb) {
+      float ka[MQ / 2], ga[MQ / 2];
+#pragma unroll
+      for (int mm = 0; mm < MQ / 2; ++mm) {
+        const int i = 2 * (hb * (MQ / 2) + mm) + i_base;
+        const int64_t row = (t0 + i) * HV + hv;
+        ka[mm] = i < Lc ? dka[row * K + d] : 0.f;
+        ga[mm] = (PER_K && i < Lc) ? dga[row * K + d] : 0.f;
+      }
+#pragma unroll
+      for (int mm = 0; mm < MQ / 2; ++mm) {
+        const int m = hb * (MQ / 2) + mm, i = 2 * m + i_base;
+        if (i >= Lc) continue;
+        const float gi = PER_K ? gam[i * GL + d] : gam[i];
+        const float eG = scan::exp_<scan::kB16<Tin>>(gi), kv = ks[i * KL + d], y = yv[m];
+        float dk = bet[i] * y * eG;
+        float dgm = dk * kv;
+        const float t1 = lo[i * KL + d], t2 = up[i * KL + d];
+        dk += t1 + t2;
+        dgm += kv * (t1 - t2);
+        dka[((t0 + i) * HV + hv) * K + d] = ka[mm] + dk;
+        gtot[i * KL + d] = PER_K ? ga[mm] + dgm : dgm;  // this thread's own entry of up
+      }
     }
   }
   __syncthreads();

@@ -138,8 +138,9 @@ __host__ __device__ constexpr int64_t prep_smem_floats(int C, int64_t K, bool pe
          prep::gram_scratch_floats(C, K, per_k);
 }
 
+// The per-key gate's shared memory allows one block an SM, the scalar gate's two.
 template <typename Tin, int C, bool PER_K>
-__global__ void __launch_bounds__(kThreads) prepare_kernel(
+__global__ void __launch_bounds__(kThreads, PER_K ? 1 : 2) prepare_kernel(
     const Tin *__restrict__ k, const Tin *__restrict__ v, const float *__restrict__ g,
     const Tin *__restrict__ beta, const int64_t *__restrict__ cu, const int64_t *__restrict__ chunk_indices,
     int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V, int l2, int beta_logits, float *__restrict__ gcum,
@@ -306,8 +307,9 @@ __host__ __device__ constexpr int64_t fwd_o_smem_floats(int C, int64_t K, bool p
          C * kOLd + prep::gram_scratch_floats(C, K, per_k);
 }
 
+// The per-key gate's shared memory allows one block an SM, the scalar gate's two.
 template <typename Tin, int C, bool PER_K>
-__global__ void __launch_bounds__(kThreads) fwd_o_kernel(
+__global__ void __launch_bounds__(kThreads, PER_K ? 1 : 2) fwd_o_kernel(
     const Tin *__restrict__ q, const Tin *__restrict__ k, const float *__restrict__ v_new,
     const float *__restrict__ h, const float *__restrict__ gcum, const int64_t *__restrict__ cu,
     const int64_t *__restrict__ chunk_indices, int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V,

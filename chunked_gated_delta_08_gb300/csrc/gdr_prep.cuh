@@ -616,21 +616,53 @@ __device__ void decayed_apply(const float *M, int lm, const float *Ylo, const fl
     __syncthreads();
     return;
   }
-  // diagonal blocks, term by term
-  for (Walk2D wk(tid, 256, (int)Kp); wk.r < C; wk.next()) {
-    const int i = wk.r;
-    const int64_t d = wk.c;
-    float a = 0.f, b = 0.f;
-    if (d < K && i < Lc) {
-      const int base = 16 * (i / 16), end = base + 16 < Lc ? base + 16 : Lc;
-      const float gi = gam[i * gl + d];
-      for (int j = base; j < end; ++j) {
-        if (STRICT ? j < i : j <= i) a = fmaf(M[i * lm + j] * Ylo[j * yl + d], scan::exp_<FAST>(gi - gam[j * gl + d]), a);
-        if (STRICT ? j > i : j >= i) b = fmaf(M[j * lm + i] * Yup[j * yl + d], scan::exp_<FAST>(gam[j * gl + d] - gi), b);
+  // diagonal blocks, term by term.  Thread (ib, d) holds column d of a block's gates and Y rows
+  // in registers (Ylo for lo, then Yup for up) and forms rows ib, ib + RP, ... of the block; the
+  // loops over the block's rows and terms are unrolled, so no term waits on a load of its own.
+  {
+    const int RP = 256 / (int)Kp;  // row phases (Kp <= 128 here)
+    const int d = tid % (int)Kp, ib = tid / (int)Kp;
+    if (ib < RP) {
+      for (int base = 0; base < C; base += 16) {
+        float yr[16], gg[16];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const int j = base + jj;
+          const bool ok = d < K && j < Lc;
+          yr[jj] = ok ? Ylo[j * yl + d] : 0.f;
+          gg[jj] = ok ? gam[j * gl + d] : 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          if (r < ib || (r - ib) % RP != 0) continue;
+          const int i = base + r;
+          float a = 0.f;
+          if (d < K && i < Lc) {
+#pragma unroll
+            for (int jj = 0; jj < (STRICT ? r : r + 1); ++jj)
+              if (base + jj < Lc) a = fmaf(M[i * lm + base + jj] * yr[jj], scan::exp_<FAST>(gg[r] - gg[jj]), a);
+          }
+          lo[i * lw + d] = a;
+        }
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const int j = base + jj;
+          yr[jj] = d < K && j < Lc ? Yup[j * yl + d] : 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          if (r < ib || (r - ib) % RP != 0) continue;
+          const int i = base + r;
+          float b = 0.f;
+          if (d < K && i < Lc) {
+#pragma unroll
+            for (int jj = STRICT ? r + 1 : r; jj < 16; ++jj)
+              if (base + jj < Lc) b = fmaf(M[(base + jj) * lm + i] * yr[jj], scan::exp_<FAST>(gg[jj] - gg[r]), b);
+          }
+          up[i * lw + d] = b;
+        }
       }
     }
-    lo[i * lw + d] = a;
-    up[i * lw + d] = b;
   }
   for (int a = 1; a < C / 16 && 16 * a < Lc; ++a) {
     const int r0 = 16 * a;
