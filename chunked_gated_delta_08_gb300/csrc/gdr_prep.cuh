@@ -571,7 +571,8 @@ __device__ void decayed_gram(const float *X, const float *Y, int64_t xl, const f
 //   up[i] += e^{G_r0 - G_i} (M[block a, i]^T (Y_r e^{G_r - G_r0}))  i < r0
 // where every exponent is non-positive for non-positive gates.  Xs, Ys:
 // scratch of gram_scratch_floats.  FAST takes the hardware exponential (bf16
-// inputs).  All 256 threads; ends with a barrier.
+// inputs); the products stay in 3 x TF32, since the gate gradients sum
+// near-cancelling terms.  All 256 threads; ends with a barrier.
 template <int C, bool PER_K, bool STRICT, bool FAST = false>
 __device__ void decayed_apply(const float *M, int lm, const float *Ylo, const float *Yup, int64_t yl, const float *gam,
                               int64_t gl, int64_t K, int Lc, float *lo, float *up, int64_t lw, float *Xs, float *Ys) {
@@ -616,14 +617,14 @@ __device__ void decayed_apply(const float *M, int lm, const float *Ylo, const fl
     __syncthreads();
     return;
   }
-  // diagonal blocks, term by term.  Thread (ib, d) holds column d of a block's gates and Y rows
-  // in registers (Ylo for lo, then Yup for up) and forms rows ib, ib + RP, ... of the block; the
-  // loops over the block's rows and terms are unrolled, so no term waits on a load of its own.
+  // diagonal blocks, term by term.  Thread (ib, d) takes column d of blocks ib, ib + RP, ...: it
+  // holds the block's gates and Y rows (Ylo for lo, then Yup for up) of that column in registers
+  // and forms all 16 rows, with the loops over rows and terms unrolled.
   {
-    const int RP = 256 / (int)Kp;  // row phases (Kp <= 128 here)
+    const int RP = 256 / (int)Kp;  // column groups (Kp <= 128 here)
     const int d = tid % (int)Kp, ib = tid / (int)Kp;
     if (ib < RP) {
-      for (int base = 0; base < C; base += 16) {
+      for (int base = 16 * ib; base < C; base += 16 * RP) {
         float yr[16], gg[16];
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
@@ -633,14 +634,13 @@ __device__ void decayed_apply(const float *M, int lm, const float *Ylo, const fl
           gg[jj] = ok ? gam[j * gl + d] : 0.f;
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          if (r < ib || (r - ib) % RP != 0) continue;
+        for (int r = 0; r < 16; ++r) {  // terms j <= i < Lc
           const int i = base + r;
           float a = 0.f;
           if (d < K && i < Lc) {
 #pragma unroll
             for (int jj = 0; jj < (STRICT ? r : r + 1); ++jj)
-              if (base + jj < Lc) a = fmaf(M[i * lm + base + jj] * yr[jj], scan::exp_<FAST>(gg[r] - gg[jj]), a);
+              a = fmaf(M[i * lm + base + jj] * yr[jj], scan::exp_<FAST>(gg[r] - gg[jj]), a);
           }
           lo[i * lw + d] = a;
         }
@@ -650,8 +650,7 @@ __device__ void decayed_apply(const float *M, int lm, const float *Ylo, const fl
           yr[jj] = d < K && j < Lc ? Yup[j * yl + d] : 0.f;
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          if (r < ib || (r - ib) % RP != 0) continue;
+        for (int r = 0; r < 16; ++r) {  // terms j >= i, j < Lc
           const int i = base + r;
           float b = 0.f;
           if (d < K && i < Lc) {
