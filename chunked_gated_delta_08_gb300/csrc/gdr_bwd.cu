@@ -338,6 +338,17 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
   const int d = tid & (kKmax - 1), i_base = tid / kKmax;
   const int ntk = (int)(Kp / 8);  // column tiles of a C x Kp product
   const int m0 = 16 * (warp % MT);
+  // the rows of a V tile into L2, one tile ahead of its loads
+  auto prefetch_tile = [&](int64_t v0) {
+    const int vb = (int)(V - v0 < 32 ? V - v0 : 32);
+    const int64_t rs = (t0 * HV + hv) * V + v0, hs0 = (chunk * HV + hv) * K * V + v0;
+    scan::prefetch_rows_l2(d_o + rs, HV * V * (int64_t)sizeof(Tin), Lc, vb * (int)sizeof(Tin));
+    scan::prefetch_rows_l2(dvn + rs, HV * V * 4, Lc, vb * 4);
+    scan::prefetch_rows_l2(v_new + rs, HV * V * 4, Lc, vb * 4);
+    scan::prefetch_rows_l2(h + hs0, V * 4, (int)K, vb * 4);
+    scan::prefetch_rows_l2(dhc + hs0, V * 4, (int)K, vb * 4);
+  };
+  prefetch_tile(0);
 
   prep::load_qk_rows<Tin, C>(q, k, t0, Lc, H, hq, K, l2, qs, ks, KQ);
   prep::tile_to_smem(gam, PER_K ? K : 1, gcum + (t0 * HV + hv) * (PER_K ? K : 1), HV * (PER_K ? K : 1), C,
@@ -358,6 +369,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dqkg_kernel(
 
   for (int64_t v0 = 0; v0 < V; v0 += 32) {
     __syncthreads();  // the previous tile's reads are done
+    if (v0 + 32 < V) prefetch_tile(v0 + 32);
     {
       // dvA holds +dv_new (dW = -dv_new h^T takes the sign when written)
       const int vok = (int)(V - v0 < 32 ? V - v0 : 32);
@@ -617,9 +629,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_wy_kernel(
   const int64_t gw = PER_K ? K : 1;
   const int d = tid & (kKmax - 1), i_base = tid / kKmax;
   const int m0 = 16 * (warp % MT);
-  // this chunk's rows of the accumulated dk (and dGamma) are read at the end: into L2 now
+  // this chunk's rows of the accumulated dk (and dGamma), dW and w are read later: into L2 now;
+  // the V tiles one tile ahead of their loads
   scan::prefetch_rows_l2(dka + (t0 * HV + hv) * K, HV * K * 4, Lc, (int)(K * 4));
   if (PER_K) scan::prefetch_rows_l2(dga + (t0 * HV + hv) * K, HV * K * 4, Lc, (int)(K * 4));
+  scan::prefetch_rows_l2(dW + (t0 * HV + hv) * K, HV * K * 4, Lc, (int)(K * 4));
+  scan::prefetch_rows_l2(w + (t0 * HV + hv) * K, HV * K * 4, Lc, (int)(K * 4));
+  auto prefetch_tile = [&](int64_t v0) {
+    const int vb = (int)(V - v0 < kWt ? V - v0 : kWt);
+    const int64_t rs = (t0 * HV + hv) * V + v0;
+    scan::prefetch_rows_l2(dvn + rs, HV * V * 4, Lc, vb * 4);
+    scan::prefetch_rows_l2(u + rs, HV * V * 4, Lc, vb * 4);
+    scan::prefetch_rows_l2(v + rs, HV * V * (int64_t)sizeof(Tin), Lc, vb * (int)sizeof(Tin));
+  };
+  prefetch_tile(0);
 
   prep::load_qk_rows<Tin, C>(nullptr, k, t0, Lc, H, hq, K, l2, nullptr, ks, KL);
   prep::tile_to_smem(gam, GL, gcum + (t0 * HV + hv) * gw, HV * gw, C, (int)gw, Lc, (int)gw);
@@ -651,6 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_wy_kernel(
   // u-path: dX = T^T dv_new per tile; dv; dbeta += rowsum(dX V); acc += dX u^T
   for (int64_t v0 = 0; v0 < V; v0 += kWt) {
     __syncthreads();
+    if (v0 + kWt < V) prefetch_tile(v0 + kWt);
     {
       const int vok = (int)(V - v0 < kWt ? V - v0 : kWt);
       prep::tile_to_smem(dvt, kLdB, dvn + (t0 * HV + hv) * V + v0, HV * V, C, kWt, Lc, vok);
