@@ -93,7 +93,8 @@ template <typename Tin, int C, bool PER_K>
 __global__ void __launch_bounds__(kThreads, PER_K ? 1 : 2) bwd_dv_local_kernel(
     const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ d_o,
     const float *__restrict__ gcum, const int64_t *__restrict__ cu, const int64_t *__restrict__ chunk_indices,
-    int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V, int l2, float *__restrict__ dvn) {
+    int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V, int l2, float *__restrict__ dvn,
+    float *__restrict__ qt_rows, float *__restrict__ kb_rows) {
   extern __shared__ float smem[];
   const int64_t Kp = scan::kpad(K), KL = Kp + 4, GL = PER_K ? Kp + 4 : 1;
   constexpr int LP = C + 4;
@@ -117,6 +118,14 @@ __global__ void __launch_bounds__(kThreads, PER_K ? 1 : 2) bwd_dv_local_kernel(
   prep::tile_to_smem(gam, GL, gcum + (t0 * HV + hv) * gw, HV * gw, C, (int)gw, Lc, (int)gw);
   for (int e = tid; e < C * LP; e += kThreads) P[e] = 0.f;  // P^T reads the upper part
   __syncthreads();
+  // Qt = q e^G and Kb = k e^{G_L - G} of the chunk's rows, read by the reverse state scan
+  for (prep::Walk2D wk(tid, kThreads, (int)K); wk.r < Lc; wk.next()) {
+    const int i = wk.r, d = wk.c;
+    const float gi = PER_K ? gam[i * GL + d] : gam[i], gl = PER_K ? gam[(Lc - 1) * GL + d] : gam[Lc - 1];
+    const int64_t at = ((t0 + i) * HV + hv) * K + d;
+    qt_rows[at] = qs[i * KL + d] * scan::exp_<scan::kB16<Tin>>(gi);
+    kb_rows[at] = ks[i * KL + d] * scan::exp_<scan::kB16<Tin>>(gl - gi);
+  }
   // P_ri = sum_d q_rd k_id exp(G_rd - G_id), i <= r < Lc
   prep::decayed_gram<C, PER_K, false, scan::kB16<Tin>, scan::kB16<Tin>>(qs, ks, KL, gam, GL, K, Lc, nullptr, P, LP,
                                                                           Xs, Ys);
@@ -142,18 +151,20 @@ __global__ void __launch_bounds__(kThreads, PER_K ? 1 : 2) bwd_dv_local_kernel(
 // --------------------------------------------------------------------------
 // dh: one block per (sequence, value head, 32-column V tile), launched longest
 // sequence first (seq_of_rank), sequential over the sequence's chunks, last
-// to first.  Per chunk, on tensor cores (3 x TF32):
+// to first.  Per chunk, on tensor cores (3 x TF32; one bf16 pass for bf16):
 //   dv_new += Kb dh'           (C x 32) = (C x K)(K x 32), Kb = k e^{G_L - G}
 //   dh = e^{G_L} dh' + Qt^T do - w^T dv_new   (K x 32),      Qt = q e^G
-// and dh' (dL/d state leaving the chunk) is recorded per chunk.
-// smem: the scan tiles (dh in hs, Kb then Qt in kt, -w in ws, dv_new in vn,
+// and dh' (dL/d state leaving the chunk) is recorded per chunk.  Kb and Qt
+// rows come formed from bwd_dv_local, so the sequential loop loads rows and
+// runs products only.
+// smem: the scan tiles (dh in hs, Kb then Qt in kt, w in ws, -dv_new in vn,
 //       G_L in gl) | dos[C][40]
 // --------------------------------------------------------------------------
 // At most 128 registers a thread, so that two blocks share an SM and every block
 // of the longest sequence is resident from the start.
 template <typename Tin, int C, bool PER_K>
 __global__ void __launch_bounds__(kThreads, 2) bwd_dh_kernel(
-    const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ d_o,
+    const float *__restrict__ qt_rows, const float *__restrict__ kb_rows, const Tin *__restrict__ d_o,
     const float *__restrict__ w, const float *__restrict__ gcum, const float *__restrict__ dht,
     const int64_t *__restrict__ cu, const int64_t *__restrict__ chunk_offsets, int64_t N, int64_t T, int64_t H,
     int64_t HV, int64_t K, int64_t V, int l2, float *__restrict__ dvn, float *__restrict__ dhc,
@@ -167,7 +178,6 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dh_kernel(
   const int64_t nvt = (V + kBVd - 1) / kBVd, per = HV * nvt;
   const int64_t n = seq_of_rank(cu, N, (int64_t)blockIdx.x / per);
   const int64_t hv = ((int64_t)blockIdx.x % per) / nvt, v0 = ((int64_t)blockIdx.x % nvt) * kBVd;
-  const int64_t hq = hv / (HV / H);
   const int64_t Kp = scan::kpad(K), WL = scan::ws_ld(K), KL = scan::kt_ld(K);
   const SeqRange sr = seq_range(cu, n, T);
   const int64_t nch = (sr.eos - sr.bos + C - 1) / C;
@@ -187,12 +197,11 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dh_kernel(
     const int64_t tl = t0 + Lc - 1;
     if (c > 0) {  // the previous chunk's rows into L2 while this one runs (it is always whole)
       const int64_t t1 = t0 - C;
-      const int64_t gwb = (PER_K ? K : 1) * 4;
       const int vb = (int)((V - v0 < kBVd ? V - v0 : kBVd));
-      scan::prefetch_rows_l2(k + (t1 * H + hq) * K, H * K * (int64_t)sizeof(Tin), C, (int)(K * sizeof(Tin)));
-      scan::prefetch_rows_l2(q + (t1 * H + hq) * K, H * K * (int64_t)sizeof(Tin), C, (int)(K * sizeof(Tin)));
+      scan::prefetch_rows_l2(kb_rows + (t1 * HV + hv) * K, HV * K * 4, C, (int)(K * 4));
+      scan::prefetch_rows_l2(qt_rows + (t1 * HV + hv) * K, HV * K * 4, C, (int)(K * 4));
       scan::prefetch_rows_l2(w + (t1 * HV + hv) * K, HV * K * 4, C, (int)(K * 4));
-      scan::prefetch_rows_l2(gcum + (t1 * HV + hv) * (PER_K ? K : 1), HV * gwb, C, (int)gwb);
+      scan::prefetch_rows_l2(gcum + ((t1 + C - 1) * HV + hv) * (PER_K ? K : 1), 4, 1, (int)(4 * (PER_K ? K : 1)));
       scan::prefetch_rows_l2(d_o + (t1 * HV + hv) * V + v0, HV * V * (int64_t)sizeof(Tin), C, vb * (int)sizeof(Tin));
       scan::prefetch_rows_l2(dvn + (t1 * HV + hv) * V + v0, HV * V * 4, C, vb * 4);
     }
@@ -202,11 +211,11 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dh_kernel(
     }
     for (int64_t d = tid; d < Kp; d += kThreads)
       st.gl[d] = d < K ? gcum[(tl * HV + hv) * gw + (PER_K ? d : 0)] : 0.f;
+    // Kb into kt, w into ws (zero past Lc and past K)
+    prep::tile_to_smem(st.kt, KL, kb_rows + (t0 * HV + hv) * K, HV * K, C, (int)Kp, Lc, (int)K);
+    prep::tile_to_smem(st.ws, WL, w + (t0 * HV + hv) * K, HV * K, C, (int)Kp, Lc, (int)K);
     __syncthreads();
-    // Kb into kt, -w into ws
-    scan::load_rows_auto<Tin, C, PER_K>(st, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
-    __syncthreads();
-    // dv_new += Kb dh'
+    // dv_new += Kb dh'; vn keeps -dv_new for the w product below
     for (int tix = warp; tix < (C / 16) * 4; tix += kWarps) {
       const int m0 = 16 * (tix % (C / 16)), n0 = 8 * (tix / (C / 16));
       float d[4];
@@ -222,30 +231,14 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dh_kernel(
         const int i = m0 + gq + 8 * (e >> 1), cc = n0 + 2 * tq + (e & 1);
         const int64_t col = v0 + cc;
         if (i < Lc && col < V) dvn[((t0 + i) * HV + hv) * V + col] = d[e];
-        st.vn[i * LD + cc] = d[e];
+        st.vn[i * LD + cc] = -d[e];
       }
     }
     __syncthreads();
     // Qt into kt (over Kb), do into dos
-    prep::load_qk_rows<Tin, C>(nullptr, q, t0, Lc, H, hq, K, l2, nullptr, st.kt, KL);
+    prep::tile_to_smem(st.kt, KL, qt_rows + (t0 * HV + hv) * K, HV * K, C, (int)Kp, Lc, (int)K);
     prep::tile_to_smem(dos, LD, d_o + (t0 * HV + hv) * V + v0, HV * V, C, kBVd, Lc,
                        (int)(V - v0 < kBVd ? V - v0 : kBVd));
-    __syncthreads();
-    // Qt = q e^G: sixteen gate loads per thread in flight at a time
-    for (prep::Walk2D wk(tid, kThreads, (int)Kp); wk.r < C;) {
-      float gv[16];
-      int rr[16], cc[16];
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        rr[u] = wk.r;
-        cc[u] = wk.c;
-        gv[u] = (wk.r < Lc && wk.c < K) ? gcum[((t0 + wk.r) * HV + hv) * gw + (PER_K ? wk.c : 0)] : 0.f;
-        wk.next();
-      }
-#pragma unroll
-      for (int u = 0; u < 16; ++u)
-        if (rr[u] < Lc && cc[u] < K) st.kt[rr[u] * KL + cc[u]] *= scan::exp_<scan::kB16<Tin>>(gv[u]);
-    }
     __syncthreads();
     // dh = e^{G_L} dh' + Qt^T do - w^T dv_new
     for (int tix = warp; tix < (int)(Kp / 16) * 4; tix += kWarps) {
@@ -918,7 +911,7 @@ int launch_bwd_dv_local(const BwdArgs &a) {
     if (rc != GDR_OK) return rc;
     kern<<<dim3((unsigned)f.nt_max, (unsigned)f.d.HV), kThreads, smem, f.stream>>>(
         (const Tin *)f.q, (const Tin *)f.k, (const Tin *)a.d_o, f.gcum, f.cu, f.chunk_indices, f.d.T, f.d.H,
-        f.d.HV, K, f.d.V, f.l2, a.dvn);
+        f.d.HV, K, f.d.V, f.l2, a.dvn, a.dqa, a.dka);  // dqa, dka are free until dqkg
     return after_launch("bwd_dv_local_kernel");
   });
 }
@@ -936,8 +929,8 @@ int launch_bwd_dh(const BwdArgs &a) {
     int rc = set_smem(kern, smem, "bwd_dh_kernel");
     if (rc != GDR_OK) return rc;
     kern<<<dim3((unsigned)(f.d.N * f.d.HV * cdiv(f.d.V, kBVd))), kThreads, smem, f.stream>>>(
-        (const Tin *)f.q, (const Tin *)f.k, (const Tin *)a.d_o, f.w, f.gcum, a.dht, f.cu, f.chunk_offsets, f.d.N,
-        f.d.T, f.d.H, f.d.HV, K, f.d.V, f.l2, a.dvn, a.dhc, a.dh0);
+        a.dqa, a.dka, (const Tin *)a.d_o, f.w, f.gcum, a.dht, f.cu, f.chunk_offsets, f.d.N, f.d.T, f.d.H,
+        f.d.HV, K, f.d.V, f.l2, a.dvn, a.dhc, a.dh0);  // Qt, Kb rows from bwd_dv_local
     return after_launch("bwd_dh_kernel");
   });
 }
