@@ -527,9 +527,37 @@ __device__ void decayed_gram(const float *X, const float *Y, int64_t xl, const f
     }
     out[i * lo + j] = acc;
   }
+  // 16-byte rows everywhere: the scaled copies move four keys at a time
+  const bool vec4 = K % 4 == 0 && xl % 4 == 0 && gl % 4 == 0 &&
+                    ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(Y) | reinterpret_cast<uintptr_t>(gam) |
+                      reinterpret_cast<uintptr_t>(Xs) | reinterpret_cast<uintptr_t>(Ys)) & 15u) == 0;
   for (int a = 1; factored && a < C / 16 && 16 * a < Lc; ++a) {
     const int r = 16 * a;
     __syncthreads();
+    if (vec4) {  // four keys per load and store
+      for (Walk2D wk(tid, 256, (int)(Kp / 4)); wk.r < 16 + r; wk.next()) {
+        const int row = wk.r;
+        const int64_t d = 4 * (int64_t)wk.c;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (row < 16) {
+          const int i = r + row;
+          if (d < K && i < Lc) {
+            const float4 x = load4(X + i * xl + d), p = load4(gam + i * gl + d), q = load4(gam + r * gl + d);
+            o = make_float4(x.x * scan::exp_<FAST>(p.x - q.x), x.y * scan::exp_<FAST>(p.y - q.y),
+                            x.z * scan::exp_<FAST>(p.z - q.z), x.w * scan::exp_<FAST>(p.w - q.w));
+          }
+          *reinterpret_cast<float4 *>(Xs + row * xl + d) = o;
+        } else {
+          const int jr = row - 16;
+          if (d < K) {
+            const float4 y = load4(Y + jr * xl + d), p = load4(gam + r * gl + d), q = load4(gam + jr * gl + d);
+            o = make_float4(y.x * scan::exp_<FAST>(p.x - q.x), y.y * scan::exp_<FAST>(p.y - q.y),
+                            y.z * scan::exp_<FAST>(p.z - q.z), y.w * scan::exp_<FAST>(p.w - q.w));
+          }
+          *reinterpret_cast<float4 *>(Ys + jr * xl + d) = o;
+        }
+      }
+    } else
     for (Walk2D wk(tid, 256, (int)Kp); wk.r < 16 + r; wk.next()) {
       const int row = wk.r;
       const int64_t d = wk.c;
@@ -663,9 +691,37 @@ __device__ void decayed_apply(const float *M, int lm, const float *Ylo, const fl
       }
     }
   }
+  // 16-byte rows everywhere: the scaled copies move four keys at a time
+  const bool vec4 = K % 4 == 0 && yl % 4 == 0 && gl % 4 == 0 &&
+                    ((reinterpret_cast<uintptr_t>(Ylo) | reinterpret_cast<uintptr_t>(Yup) | reinterpret_cast<uintptr_t>(gam) |
+                      reinterpret_cast<uintptr_t>(Xs) | reinterpret_cast<uintptr_t>(Ys)) & 15u) == 0;
   for (int a = 1; a < C / 16 && 16 * a < Lc; ++a) {
     const int r0 = 16 * a;
     __syncthreads();
+    if (vec4) {  // four keys per load and store
+      for (Walk2D wk(tid, 256, (int)(Kp / 4)); wk.r < 16 + r0; wk.next()) {
+        const int row = wk.r;
+        const int64_t d = 4 * (int64_t)wk.c;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (row < 16) {
+          const int r = r0 + row;
+          if (d < K && r < Lc) {
+            const float4 y = load4(Yup + r * yl + d), p = load4(gam + r * gl + d), q = load4(gam + r0 * gl + d);
+            o = make_float4(y.x * scan::exp_<FAST>(p.x - q.x), y.y * scan::exp_<FAST>(p.y - q.y),
+                            y.z * scan::exp_<FAST>(p.z - q.z), y.w * scan::exp_<FAST>(p.w - q.w));
+          }
+          *reinterpret_cast<float4 *>(Xs + row * yl + d) = o;
+        } else {
+          const int j = row - 16;
+          if (d < K) {
+            const float4 y = load4(Ylo + j * yl + d), p = load4(gam + r0 * gl + d), q = load4(gam + j * gl + d);
+            o = make_float4(y.x * scan::exp_<FAST>(p.x - q.x), y.y * scan::exp_<FAST>(p.y - q.y),
+                            y.z * scan::exp_<FAST>(p.z - q.z), y.w * scan::exp_<FAST>(p.w - q.w));
+          }
+          *reinterpret_cast<float4 *>(Ys + j * yl + d) = o;
+        }
+      }
+    } else
     for (Walk2D wk(tid, 256, (int)Kp); wk.r < 16 + r0; wk.next()) {
       const int row = wk.r;
       const int64_t d = wk.c;
