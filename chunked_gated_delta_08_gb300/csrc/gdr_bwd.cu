@@ -114,6 +114,8 @@ __global__ void __launch_bounds__(kThreads, PER_K ? 1 : 2) bwd_dv_local_kernel(
   const int64_t hq = hv / (HV / H);
   const int64_t gw = PER_K ? K : 1;
 
+  // the chunk's d_o rows, read tile by tile after the Gram: into L2 now
+  scan::prefetch_rows_l2(d_o + (t0 * HV + hv) * V, HV * V * (int64_t)sizeof(Tin), Lc, (int)(V * sizeof(Tin)));
   prep::load_qk_rows<Tin, C>(q, k, t0, Lc, H, hq, K, l2, qs, ks, KL);
   prep::tile_to_smem(gam, GL, gcum + (t0 * HV + hv) * gw, HV * gw, C, (int)gw, Lc, (int)gw);
   for (int e = tid; e < C * LP; e += kThreads) P[e] = 0.f;  // P^T reads the upper part

@@ -168,6 +168,8 @@ __global__ void __launch_bounds__(kThreads, PER_K ? 1 : 2) prepare_kernel(
   const int nk = (int)(Kp / 8);
   (void)nk;
 
+  // the chunk's v rows, read tile by tile after the solve: into L2 now
+  scan::prefetch_rows_l2(v + (t0 * HV + hv) * V, HV * V * (int64_t)sizeof(Tin), Lc, (int)(V * sizeof(Tin)));
   // ---- k rows (normalized), g, beta
   prep::load_qk_rows<Tin, C>(nullptr, k, t0, Lc, H, hq, K, l2, nullptr, ks, KL);
   prep::tile_to_smem(gam, GL, g + (t0 * HV + hv) * gw, HV * gw, C, (int)gw, Lc, (int)gw);
