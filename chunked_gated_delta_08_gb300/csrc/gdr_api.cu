@@ -103,6 +103,13 @@ void sizes_of(const gdr_desc &d, int C, const int64_t *cu, gdr_chunked_sizes *s)
   s->h_bytes = sizeof(float) * (size_t)(s->nt_max * d.HV * d.K * d.V);
 }
 
+// Whether prepare may form k e^{G_L - G} for the state scan: only where prepare's q/k row loader and
+// the scan's row loader both take their vector forms (K % 4 == 0, K <= 128, k 16-byte aligned), so
+// the formed rows equal the ones the scan would form, bit for bit.
+bool kb_formable(const gdr_desc &d, const void *k) {
+  return d.K % 4 == 0 && d.K <= 128 && (reinterpret_cast<uintptr_t>(k) & 15u) == 0;
+}
+
 int run_chunked(const gdr_desc &d, const void *q, const void *k, const void *v, const float *g, const void *beta,
                 const float *h0, const int64_t *cu, int C, int l2, void *o, float *ht, cudaStream_t stream) {
   int dev, rc;
@@ -120,7 +127,9 @@ int run_chunked(const gdr_desc &d, const void *q, const void *k, const void *v, 
                           align256(s.w_bytes),
                           align256(s.u_bytes),
                           align256(s.v_new_bytes)};
-  size_t total = align256(s.h_bytes);
+  // k e^{G_L - G} formed once by prepare for the state scan, where both take their vector row loaders
+  const bool formed_kb = kb_formable(d, k);
+  size_t total = align256(s.h_bytes) + (formed_kb ? align256(s.w_bytes) : 0);
   for (size_t x : offs) total += x;
   char *base = nullptr;
   cudaError_t e = cudaMallocFromPoolAsync((void **)&base, total > 0 ? total : 256, pool, stream);
@@ -137,7 +146,8 @@ int run_chunked(const gdr_desc &d, const void *q, const void *k, const void *v, 
   a.w = (float *)p; p += offs[4];
   a.u = (float *)p; p += offs[5];
   a.v_new = (float *)p; p += offs[6];
-  a.h = (float *)p;
+  a.h = (float *)p; p += align256(s.h_bytes);
+  a.kb = formed_kb ? (float *)p : nullptr;
   a.ht = ht;
   a.o = o;
   a.nt_max = s.nt_max;
@@ -319,6 +329,7 @@ int run_bwd(const gdr_desc &d, const void *q, const void *k, const void *v, cons
   b.dga = (float *)ptr[11];
   b.dW = (float *)ptr[12];
   b.dq = dq; b.dk = dk; b.dv = dv; b.dbeta = dbeta; b.dg = dg; b.dh0 = dh0;
+  a.kb = kb_formable(d, k) ? b.dka : nullptr;  // free until dqkg (dv_local writes the same rows there)
   if (cu) rc = launch_chunk_index(a);
   if (rc == GDR_OK) rc = launch_chunk_prepare(a);
   if (rc == GDR_OK) rc = launch_chunk_fwd_h(a);

@@ -144,7 +144,8 @@ __global__ void __launch_bounds__(kThreads, PER_K ? 1 : 2) prepare_kernel(
     const Tin *__restrict__ k, const Tin *__restrict__ v, const float *__restrict__ g,
     const Tin *__restrict__ beta, const int64_t *__restrict__ cu, const int64_t *__restrict__ chunk_indices,
     int64_t T, int64_t H, int64_t HV, int64_t K, int64_t V, int l2, int beta_logits, float *__restrict__ gcum,
-    float *__restrict__ w, float *__restrict__ u) {
+    float *__restrict__ w, float *__restrict__ u,
+    float *__restrict__ kb_rows) {
   extern __shared__ float smem[];
   const int64_t Kp = scan::kpad(K), KL = Kp + 4, GL = PER_K ? Kp + 4 : 1;
   constexpr int LA = C + 1, LT = C + 4;
@@ -185,6 +186,12 @@ __global__ void __launch_bounds__(kThreads, PER_K ? 1 : 2) prepare_kernel(
   __syncthreads();
   for (prep::Walk2D wk(tid, kThreads, (int)gw); wk.r < Lc; wk.next())
     gcum[((t0 + wk.r) * HV + hv) * gw + wk.c] = gam[wk.r * GL + wk.c];
+  if (kb_rows)  // k e^{G_L - G} for the state scan, formed once instead of in each of its V-tile blocks
+    for (prep::Walk2D wk(tid, kThreads, (int)K); wk.r < Lc; wk.next()) {
+      const int i = wk.r, d = wk.c;
+      const float gi = PER_K ? gam[i * GL + d] : gam[i], gl = PER_K ? gam[(Lc - 1) * GL + d] : gam[Lc - 1];
+      kb_rows[((t0 + i) * HV + hv) * K + d] = ks[i * KL + d] * scan::exp_<scan::kB16<Tin>>(gl - gi);
+    }
 
   // ---- A (strictly lower) into AT
   prep::decayed_gram<C, PER_K, true, scan::kB16<Tin>>(ks, ks, KL, gam, GL, K, Lc, bet, AT, LA, Xs, Ys);
@@ -246,12 +253,14 @@ __global__ void __launch_bounds__(kThreads, PER_K ? 1 : 2) prepare_kernel(
 // longest sequence first (seq_of_rank), sequential over the sequence's chunks.
 // Each chunk's two products run on tensor cores in 3 x TF32 (gdr_scan.cuh).
 // --------------------------------------------------------------------------
+// At most 128 registers a thread: two blocks share an SM (the longest sequence's blocks in one wave).
 template <typename Tin, int C, bool PER_K>
-__global__ void __launch_bounds__(kThreads) fwd_h_kernel(
+__global__ void __launch_bounds__(kThreads, 2) fwd_h_kernel(
     const Tin *__restrict__ k, const float *__restrict__ w, const float *__restrict__ u,
     const float *__restrict__ gcum, const float *__restrict__ h0, const int64_t *__restrict__ cu,
     const int64_t *__restrict__ chunk_offsets, int64_t N, int64_t T, int64_t H, int64_t HV, int64_t K,
-    int64_t V, int l2, float *__restrict__ h, float *__restrict__ v_new, float *__restrict__ ht) {
+    int64_t V, int l2, float *__restrict__ h, float *__restrict__ v_new, float *__restrict__ ht,
+    const float *__restrict__ kb_rows) {
   extern __shared__ float smem[];
   const scan::Tiles st = scan::carve(smem, C, K);
   if (chunk_offsets && chunk_offsets[N] < 0) return;
@@ -280,7 +289,7 @@ __global__ void __launch_bounds__(kThreads) fwd_h_kernel(
         const int64_t d = e / kBVh, vv = e % kBVh;
         if (v0 + vv < V) h[(((cbase + c) * HV + hv) * K + d) * V + v0 + vv] = st.hs[d * scan::kHS + vv];
       }
-    scan::chunk_step<Tin, C, PER_K>(st, k, w, u, gcum, t0, Lc, hv, hq, H, HV, K, V, V, v0, l2, v_new);
+    scan::chunk_step<Tin, C, PER_K>(st, k, w, u, gcum, t0, Lc, hv, hq, H, HV, K, V, V, v0, l2, v_new, kb_rows);
   }
   if (ht)
     for (int64_t e = tid; e < K * kBVh; e += kThreads) {
@@ -447,7 +456,7 @@ static int prepare_t(const ChunkedArgs &a) {
     if (rc == GDR_OK && a.nt_max > 0) {
       kern<<<grid, kThreads, smem, a.stream>>>((const Tin *)a.k, (const Tin *)a.v, a.g, (const Tin *)a.beta, a.cu,
                                                a.chunk_indices, a.d.T, a.d.H, a.d.HV, K, V, a.l2,
-                                               (a.d.flags & GDR_FLAG_BETA_LOGITS) ? 1 : 0, a.gcum, a.w, a.u);
+                                               (a.d.flags & GDR_FLAG_BETA_LOGITS) ? 1 : 0, a.gcum, a.w, a.u, a.kb);
       rc = check_launch("prepare_kernel");
     }
     return rc;
@@ -466,7 +475,7 @@ static int fwd_h_t(const ChunkedArgs &a) {
     int rc = launch_checked(kern, grid, smem, a.stream, "fwd_h_kernel");
     if (rc == GDR_OK && a.d.N > 0) {
       kern<<<grid, kThreads, smem, a.stream>>>((const Tin *)a.k, a.w, a.u, a.gcum, a.h0, a.cu, a.chunk_offsets,
-                                               a.d.N, a.d.T, a.d.H, a.d.HV, K, V, a.l2, a.h, a.v_new, a.ht);
+                                               a.d.N, a.d.T, a.d.H, a.d.HV, K, V, a.l2, a.h, a.v_new, a.ht, a.kb);
       rc = check_launch("fwd_h_kernel");
     }
     return rc;

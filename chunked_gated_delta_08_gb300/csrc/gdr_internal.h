@@ -39,6 +39,7 @@ struct ChunkedArgs {
   const int64_t *cu;
   int64_t *chunk_indices, *chunk_offsets;  // may be null in the dense layout
   float *gcum, *w, *u, *h, *v_new, *ht;
+  float *kb;  // nullable: k e^{G_L - G} rows [B*T, HV, K] fp32, formed by prepare, read by fwd_h
   void *o;
   int64_t nt_max;
   int *status;

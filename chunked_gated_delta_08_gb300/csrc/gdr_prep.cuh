@@ -378,8 +378,9 @@ __device__ __forceinline__ void load_qk_rows_vec(const Tin *__restrict__ q, cons
 #pragma unroll
   for (int r = 0; r < RPW; ++r) {
     const int i = warp + kWarps * r;
-    const float sq = qv[r].x * qv[r].x + qv[r].y * qv[r].y + qv[r].z * qv[r].z + qv[r].w * qv[r].w;
-    const float sk = kv[r].x * kv[r].x + kv[r].y * kv[r].y + kv[r].z * kv[r].z + kv[r].w * kv[r].w;
+    // the lane's partial sums in the scan's row loader's order, so both normalize a row alike
+    const float sq = fmaf(qv[r].w, qv[r].w, fmaf(qv[r].z, qv[r].z, fmaf(qv[r].y, qv[r].y, fmaf(qv[r].x, qv[r].x, 0.f))));
+    const float sk = fmaf(kv[r].w, kv[r].w, fmaf(kv[r].z, kv[r].z, fmaf(kv[r].y, kv[r].y, fmaf(kv[r].x, kv[r].x, 0.f))));
     const float cq = l2 ? rsqrtf(warp_sum(sq) + kL2Eps) : 1.f, ck = l2 ? rsqrtf(warp_sum(sk) + kL2Eps) : 1.f;
     if (d0 < width) {  // zero past K up to the padded width
       if (q) *reinterpret_cast<float4 *>(qs + i * xl + d0) = make_float4(qv[r].x * cq, qv[r].y * cq, qv[r].z * cq, qv[r].w * cq);

@@ -250,6 +250,56 @@ __device__ __forceinline__ void load_rows_vec(const Tiles &s, const Tin *__restr
   }
 }
 
+// Kb rows already formed (k e^{G_L - G}, by prepare) and -w, for K % 4 == 0,
+// K <= 128 and 16-byte aligned rows: lane l takes keys 4l .. 4l + 3, four rows
+// per warp in flight.  Writes G_L per key into s.gl, visible to the block
+// after the caller's next barrier.
+template <int C, bool PER_K>
+__device__ __forceinline__ void load_rows_formed(const Tiles &s, const float *__restrict__ kb,
+                                                 const float *__restrict__ w, const float *__restrict__ gcum,
+                                                 int64_t t0, int Lc, int64_t hv, int64_t HV, int64_t K) {
+  constexpr int kWarps = kScanThreads / 32;
+  constexpr int RPW = C / kWarps, RB = 4;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t Kp = kpad(K), WL = ws_ld(K), KL = kt_ld(K);
+  const int d0 = 4 * lane;
+  const bool lane_in = d0 < K;
+  if (warp == 0 && d0 < Kp) {
+    const int64_t tl = t0 + Lc - 1;
+    float4 gl = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane_in) {
+      if (PER_K) {
+        gl = *reinterpret_cast<const float4 *>(gcum + (tl * HV + hv) * K + d0);
+      } else {
+        const float x = gcum[tl * HV + hv];
+        gl = make_float4(x, x, x, x);
+      }
+    }
+    *reinterpret_cast<float4 *>(s.gl + d0) = gl;
+  }
+#pragma unroll
+  for (int jb = 0; jb < RPW; jb += RB) {
+    float4 kv[RB], wv[RB];
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      const int i = warp + kWarps * (jb + r);
+      const bool ok = lane_in && i < Lc;
+      const int64_t off = ((t0 + i) * HV + hv) * K + d0;
+      kv[r] = ok ? *reinterpret_cast<const float4 *>(kb + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+      wv[r] = ok ? *reinterpret_cast<const float4 *>(w + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      if (jb + r >= RPW) break;
+      const int i = warp + kWarps * (jb + r);
+      if (d0 < Kp) {
+        *reinterpret_cast<float4 *>(s.kt + i * KL + d0) = kv[r];
+        *reinterpret_cast<float4 *>(s.ws + i * WL + d0) = make_float4(-wv[r].x, -wv[r].y, -wv[r].z, -wv[r].w);
+      }
+    }
+  }
+}
+
 // The row loader for the shape: vector loads where K % 4 == 0, K <= 128 and
 // k, w, gcum are 16-byte aligned (every row then starts on a 16-byte, bf16 k
 // an 8-byte, boundary), else the scalar loaders.
@@ -276,7 +326,7 @@ __device__ __forceinline__ void chunk_step(const Tiles &s, const Tin *__restrict
                                            const float *__restrict__ u, const float *__restrict__ gcum,
                                            int64_t t0, int Lc, int64_t hv, int64_t hq, int64_t H, int64_t HV,
                                            int64_t K, int64_t V, int64_t ucols, int64_t c0col, int l2,
-                                           float *__restrict__ v_new_out) {
+                                           float *__restrict__ v_new_out, const float *__restrict__ kb_rows = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, tq = lane & 3;
   const int64_t Kp = kpad(K), WL = ws_ld(K), KL = kt_ld(K);
@@ -297,7 +347,9 @@ __device__ __forceinline__ void chunk_step(const Tiles &s, const Tin *__restrict
       }
   }
   // Kb and -w, zero past Lc and past K; G_L per key into s.gl
-  if (rows_vec_ok(k, w, gcum, K)) {
+  if (kb_rows && rows_vec_ok(kb_rows, w, gcum, K)) {
+    load_rows_formed<C, PER_K>(s, kb_rows, w, gcum, t0, Lc, hv, HV, K);
+  } else if (rows_vec_ok(k, w, gcum, K)) {
     load_rows_vec<Tin, C, PER_K>(s, k, w, gcum, t0, Lc, hv, hq, H, HV, K, l2);
   } else {
     for (int64_t d = tid; d < Kp; d += kScanThreads)
