@@ -1,5 +1,7 @@
-// gdr_bwd.cu -- the backward of the chunked gated delta rule on CUDA cores,
-// fp32 arithmetic throughout.
+// gdr_bwd.cu -- the backward of the chunked gated delta rule.  Products run on
+// warp-level tensor-core MMAs with fp32 accumulation: 3 x TF32 for fp32
+// inputs; for bf16 inputs the Gram matrices, the solves and the decayed
+// products of the gate gradients in 3 x TF32, the rest in one bf16 pass.
 //
 // The pages give the backward as a chain of chunk kernels (KCP handbook, the
 // debug-script layout: bwd_dAu -> bwd_dhu -> bwd_dv -> bwd_o -> bwd_wy ->
@@ -12,7 +14,8 @@
 //             T = (I + A)^-1,  A_ij = b_i sum_d k_id k_jd e^(G_id - G_jd) (i > j)
 //             h' = e^(G_L) h + Kb^T v_new,  Kb = K e^(G_L - G)
 //             o  = Qt h + P v_new,  Qt = Q e^G,  P_ri = sum_d q_rd k_id e^(G_rd - G_id) (i <= r)
-//   backward: dv_new = P^T do + Kb dh'                      (bwd_dv_local_kernel, bwd_dh_kernel)
+//   backward: dv_new = P^T do + Kb dh'                      (bwd_dv_local_kernel, bwd_dh_kernel;
+//                                                             dv_local also forms the Qt, Kb rows)
 //             dh     = Qt^T do + e^(G_L) dh' - w^T dv_new    (bwd_dh_kernel, reverse over chunks)
 //             dQt = do h^T,  dW = -dv_new h^T,  dKb = v_new dh'^T,  dP = do v_new^T
 //                                                            (bwd_dqkg_kernel)

@@ -1,5 +1,5 @@
 // gdr_chunked.cu -- the chunked (three-kernel) form of the gated delta rule
-// forward on CUDA cores, fp32 arithmetic throughout.
+// forward, products on warp-level tensor-core MMAs with fp32 accumulation.
 //
 // Kernel order follows the pages' forward chain (KCP handbook, section on the
 // debug-script layout: fwd_intra -> wy -> fwd_h -> o):
@@ -7,14 +7,16 @@
 //   prepare_kernel      per (chunk, value head): L2 norm of k, gate cumsum,
 //                       A = tril(beta K K^T * decay, -1), T = (I + A)^-1 by
 //                       blocks (tensor cores, 3 x TF32), w and u as products
-//                       with T
+//                       with T; when given a buffer, also the rows
+//                       K * exp(G_C - G) for the state scan
 //   fwd_h_kernel        per (sequence, value head, V-tile), sequential over
 //                       chunks: h (state entering the chunk), v_new = u - w h,
 //                       h <- exp(G_C) h + (K * exp(G_C - G))^T v_new, both
-//                       products on tensor cores in 3 x TF32 (gdr_scan.cuh)
+//                       products on tensor cores (gdr_scan.cuh); the rows
+//                       K * exp(G_C - G) read as formed by prepare, or formed
 //   fwd_o_kernel        per (chunk, value head): o = (q * exp G) h + P v_new
 //                       with P = tril(q k^T * decay) (diagonal included),
-//                       on tensor cores (3 x TF32)
+//                       on tensor cores
 //
 // Decay factors are always formed as exp(G_i - G_j) with i >= j, so every
 // exponent is <= 0 and nothing overflows, whatever the gate values.
