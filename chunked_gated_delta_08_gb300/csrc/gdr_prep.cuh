@@ -1,6 +1,7 @@
 // gdr_prep.cuh -- tensor-core building blocks of the chunked form's
 // per-chunk preparation: 16 x 8 warp tiles of shared-memory products in
-// 3 x TF32 (close to fp32), and T = (I + A)^-1 of a unit lower-triangular
+// 3 x TF32 (close to fp32) or one bf16 pass, the decayed Gram and decayed
+// products of the per-key gate, and T = (I + A)^-1 of a unit lower-triangular
 // C x C matrix by blocks (the UT transform behind the WY representation of
 // the coverage guide, section 二).
 //

@@ -1,5 +1,6 @@
 // gdr_scan.cuh -- one chunk of the state scan on a 32-column tile, with both
-// of its products on warp-level tensor-core MMAs in 3 x TF32 (close to fp32).
+// of its products on warp-level tensor-core MMAs: 3 x TF32 (close to fp32)
+// for fp32 inputs, one bf16 pass (m16n8k16, fp32 accumulation) for bf16.
 //
 // For the chunk starting at token t0 with Lc valid rows, h the K x 32 state
 // tile entering it (shared memory), Gamma the gate cumsum and L the last
