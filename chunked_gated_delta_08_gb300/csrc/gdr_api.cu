@@ -329,7 +329,7 @@ int run_bwd(const gdr_desc &d, const void *q, const void *k, const void *v, cons
   b.dga = (float *)ptr[11];
   b.dW = (float *)ptr[12];
   b.dq = dq; b.dk = dk; b.dv = dv; b.dbeta = dbeta; b.dg = dg; b.dh0 = dh0;
-  a.kb = kb_formable(d, k) ? b.dka : nullptr;  // free until dqkg (dv_local writes the same rows there)
+  a.kb = kb_formable(d, k) ? b.dka : nullptr;  // free until dqkg; the reverse scan reads these rows too
   if (cu) rc = launch_chunk_index(a);
   if (rc == GDR_OK) rc = launch_chunk_prepare(a);
   if (rc == GDR_OK) rc = launch_chunk_fwd_h(a);

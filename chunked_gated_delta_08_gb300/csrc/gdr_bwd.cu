@@ -123,13 +123,17 @@ __global__ void __launch_bounds__(kThreads, PER_K ? 1 : 2) bwd_dv_local_kernel(
   prep::tile_to_smem(gam, GL, gcum + (t0 * HV + hv) * gw, HV * gw, C, (int)gw, Lc, (int)gw);
   for (int e = tid; e < C * LP; e += kThreads) P[e] = 0.f;  // P^T reads the upper part
   __syncthreads();
-  // Qt = q e^G and Kb = k e^{G_L - G} of the chunk's rows, read by the reverse state scan
+  // Qt = q e^G and (unless prepare formed them already: kb_rows null) Kb = k e^{G_L - G} of the
+  // chunk's rows, read by the reverse state scan
   for (prep::Walk2D wk(tid, kThreads, (int)K); wk.r < Lc; wk.next()) {
     const int i = wk.r, d = wk.c;
-    const float gi = PER_K ? gam[i * GL + d] : gam[i], gl = PER_K ? gam[(Lc - 1) * GL + d] : gam[Lc - 1];
+    const float gi = PER_K ? gam[i * GL + d] : gam[i];
     const int64_t at = ((t0 + i) * HV + hv) * K + d;
     qt_rows[at] = qs[i * KL + d] * scan::exp_<scan::kB16<Tin>>(gi);
-    kb_rows[at] = ks[i * KL + d] * scan::exp_<scan::kB16<Tin>>(gl - gi);
+    if (kb_rows) {
+      const float gl = PER_K ? gam[(Lc - 1) * GL + d] : gam[Lc - 1];
+      kb_rows[at] = ks[i * KL + d] * scan::exp_<scan::kB16<Tin>>(gl - gi);
+    }
   }
   // P_ri = sum_d q_rd k_id exp(G_rd - G_id), i <= r < Lc
   prep::decayed_gram<C, PER_K, false, scan::kB16<Tin>, scan::kB16<Tin>>(qs, ks, KL, gam, GL, K, Lc, nullptr, P, LP,
@@ -916,7 +920,8 @@ int launch_bwd_dv_local(const BwdArgs &a) {
     if (rc != GDR_OK) return rc;
     kern<<<dim3((unsigned)f.nt_max, (unsigned)f.d.HV), kThreads, smem, f.stream>>>(
         (const Tin *)f.q, (const Tin *)f.k, (const Tin *)a.d_o, f.gcum, f.cu, f.chunk_indices, f.d.T, f.d.H,
-        f.d.HV, K, f.d.V, f.l2, a.dvn, a.dqa, a.dka);  // dqa, dka are free until dqkg
+        f.d.HV, K, f.d.V, f.l2, a.dvn, a.dqa, f.kb ? nullptr : a.dka);  // dqa, dka are free until dqkg;
+                                                                       // f.kb (== dka) already holds Kb
     return after_launch("bwd_dv_local_kernel");
   });
 }
